@@ -1,0 +1,100 @@
+"""Seeded synthetic attention inputs.
+
+This module is the only code that both the fp64 oracle tests and the CUDA-path
+tests import. It draws numbers and rounds them to the storage dtype; it holds
+none of the attention arithmetic.
+
+Recipe (the pages only ever feed random normal tensors to their kernels:
+"How I profile" and "The sweep" on the profile-driven FlashAttention-2 page,
+and the correctness grid on the gpu-attention-phase1-phase2 page):
+
+* one CPU ``torch.Generator`` seeded per workload, drawing Q, then K, then V,
+  each ``randn`` in fp32 with shape ``[B, H, N, d]``;
+* an optional exact multiply by a power of two (the wide-head long-sequence
+  workload uses 2, to push the running row maximum around);
+* one round-to-nearest-even cast to fp16 or bf16.
+
+The rounded 16-bit tensors are what both sides consume.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional, Tuple
+
+import torch
+
+_DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+def to_dtype(name: str) -> torch.dtype:
+    try:
+        return _DTYPES[name]
+    except KeyError:
+        raise ValueError(f"unknown dtype {name!r}; expected one of {sorted(_DTYPES)}")
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One named problem: shapes, dtypes, masks, input scale and seed."""
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtypes: Tuple[str, ...]
+    causal: Tuple[bool, ...]
+    input_scale: float
+    seed: int
+
+
+# The fixed problems this library is measured and checked on. Seeds are fixed
+# per problem so that every run draws the same tensors.
+WORKLOADS: List[Workload] = [
+    Workload("b1h1n128d64", 1, 1, 128, 64, ("fp16",), (False,), 1.0, 61000),
+    Workload("b2h4n1000d64", 2, 4, 1000, 64, ("fp16", "bf16"), (False, True), 1.0, 61001),
+    Workload("b4h16n4096d64", 4, 16, 4096, 64, ("bf16",), (False, True), 1.0, 61002),
+    Workload("b1h16n8192d128x2", 1, 16, 8192, 128, ("bf16",), (True,), 2.0, 61003),
+]
+
+
+def workload(name: str) -> Workload:
+    for w in WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384)
+SWEEP_D = (64, 128)
+
+
+def sweep_seed(N: int, d: int, dtype: str, causal: bool) -> int:
+    """Seed of one sequence-sweep point, derived from its parameters."""
+    return 61004 + 1000 * SWEEP_N.index(N) + 100 * SWEEP_D.index(d) + \
+        10 * ("fp16", "bf16").index(dtype) + int(causal)
+
+
+def sweep_points():
+    """Every point of the sequence sweep: B = 16384/N, H = 16."""
+    for N in SWEEP_N:
+        for d in SWEEP_D:
+            for dtype in ("fp16", "bf16"):
+                for causal in (False, True):
+                    yield dict(B=16384 // N, H=16, N=N, d=d, dtype=dtype, causal=causal,
+                               seed=sweep_seed(N, d, dtype, causal))
+
+
+def make_qkv(B: int, H: int, N: int, d: int, dtype: str, seed: int,
+             input_scale: float = 1.0, generator: Optional[torch.Generator] = None):
+    """Draw Q, K, V ~ N(0,1) (times ``input_scale``) in fp32 and round to ``dtype``.
+
+    Returns three contiguous CPU tensors of shape [B, H, N, d].
+    """
+    g = generator if generator is not None else torch.Generator().manual_seed(int(seed))
+    out = []
+    for _ in range(3):
+        x = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+        if input_scale != 1.0:
+            x.mul_(input_scale)
+        out.append(x.to(to_dtype(dtype)).contiguous())
+    return tuple(out)

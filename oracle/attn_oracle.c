@@ -1,0 +1,146 @@
+/*
+ * fp64 CPU oracle for the exact scaled-dot-product attention forward.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg load this library; the product path never does.
+ * It shares no source, header or helper with the CUDA path.
+ *
+ * What it computes is the plain definition of the method, written out once per
+ * query row (no tiling, no online rescaling, no reordering):
+ *
+ *   visible set   V_i = { j : 0 <= j < N  and, under the causal mask, j <= i }
+ *   scores        s_j = scale * sum_t q[i,t] * k[j,t]            (j in V_i)
+ *   stable soft-  m   = max_j s_j,  e_j = exp(s_j - m),  l = sum_j e_j
+ *   max
+ *   output        O[i,:] = sum_j e_j * v[j,:] / l
+ *   logsumexp     LSE[i] = m + ln(l)          (natural log of the scaled scores)
+ *
+ * Passages followed:
+ *  - "Programming an attention kernel in Triton", Kernel 3 (fused softmax):
+ *    subtract the row max, exponentiate, sum, divide.
+ *  - same page, Kernel 4 (a self-attention kernel): scores = scale * Q K^T over
+ *    the keys inside the sequence, softmax along the key axis, weights times V.
+ *  - "如何用 profiler 逐步优化 Triton FlashAttention-2 kernel" (profile-driven
+ *    FlashAttention-2 page), Round 4 / Causal tile-skipping: a key is kept iff
+ *    k_pos < N_KEYS and, when causal, k_pos <= q_pos (top-left aligned).
+ *  - same page, Round 4 / exp2: L is reported in natural-log units and must
+ *    equal torch.logsumexp of the scaled scores.
+ *
+ * Inputs are fp64 arrays, row-major [B*H][N][d]; callers upcast the 16-bit
+ * tensors exactly before the call. Every row has at least one visible key
+ * (key 0, and key i itself under the causal mask), so m and l are finite.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* One query row i of one head. K and V point at that head's [N][d] block.
+ * s is scratch of at least N doubles. */
+static void oracle_row(const double* qi, const double* K, const double* V,
+                       int64_t N, int64_t d, int64_t i, int causal, double scale,
+                       double* s, double* oi, double* lse_i)
+{
+    const int64_t n_vis = causal ? (i + 1 < N ? i + 1 : N) : N;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        const double* kj = K + j * d;
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t) dot += qi[t] * kj[t];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        s[j] = exp(s[j] - m);
+        l += s[j];
+    }
+    for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        const double e = s[j];
+        const double* vj = V + j * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] += e * vj[t];
+    }
+    for (int64_t t = 0; t < d; ++t) oi[t] /= l;
+    *lse_i = m + log(l);
+}
+
+static int bad_args(const void* q, const void* k, const void* v, const void* o,
+                    const void* lse, int64_t BH, int64_t N, int64_t d, double scale)
+{
+    if (!q || !k || !v || !o || !lse) return 1;
+    if (BH < 1 || N < 1 || d < 1) return 1;
+    if (!(scale > 0.0) || !isfinite(scale)) return 1;
+    return 0;
+}
+
+/* Full forward: o[BH][N][d], lse[BH][N]. Returns 0, or -1 on bad arguments,
+ * or -2 when scratch memory cannot be had. */
+int oracle_attn_fwd(const double* q, const double* k, const double* v,
+                    double* o, double* lse, int64_t B, int64_t H, int64_t N,
+                    int64_t d, int causal, double scale)
+{
+    const int64_t BH = B * H;
+    if (B < 1 || H < 1 || bad_args(q, k, v, o, lse, BH, N, d, scale)) return -1;
+    int failed = 0;
+#pragma omp parallel reduction(| : failed)
+    {
+        double* s = (double*)malloc((size_t)N * sizeof(double));
+        if (!s) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 16) collapse(2)
+            for (int64_t bh = 0; bh < BH; ++bh) {
+                for (int64_t i = 0; i < N; ++i) {
+                    const double* base_q = q + (bh * N + i) * d;
+                    oracle_row(base_q, k + bh * N * d, v + bh * N * d, N, d, i, causal, scale,
+                               s, o + (bh * N + i) * d, lse + bh * N + i);
+                }
+            }
+            free(s);
+        }
+    }
+    return failed ? -2 : 0;
+}
+
+/* Selected rows only: rows[r] is the flat index bh*N + i. Outputs are packed:
+ * o[r][d], lse[r]. Used to check sampled outputs of workloads too large to
+ * recompute whole. */
+int oracle_attn_rows(const double* q, const double* k, const double* v,
+                     int64_t BH, int64_t N, int64_t d, int causal, double scale,
+                     const int64_t* rows, int64_t nrows, double* o, double* lse)
+{
+    if (!rows || nrows < 0 || bad_args(q, k, v, o, lse, BH, N, d, scale)) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= BH * N) return -1;
+    int failed = 0;
+#pragma omp parallel reduction(| : failed)
+    {
+        double* s = (double*)malloc((size_t)N * sizeof(double));
+        if (!s) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < nrows; ++r) {
+                const int64_t bh = rows[r] / N, i = rows[r] % N;
+                oracle_row(q + rows[r] * d, k + bh * N * d, v + bh * N * d, N, d, i, causal,
+                           scale, s, o + r * d, lse + r);
+            }
+            free(s);
+        }
+    }
+    return failed ? -2 : 0;
+}
+
+/* Threads an OpenMP parallel region of this library uses. */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
