@@ -1,0 +1,498 @@
+// Fused exact attention forward for sm_103a: TMA-fed K/V ring, tcgen05 MMAs
+// accumulating in tensor memory, warp-specialised load / MMA / softmax roles.
+//
+// What it computes, per head and query row i (natural-log LSE):
+//   O[i] = sum_{j visible} softmax_j(scale * q_i.k_j) v_j,  LSE[i] = ln sum_j exp(scale*q_i.k_j)
+// following the tiled online-softmax forward of "如何用 profiler 逐步优化 Triton
+// FlashAttention-2 kernel" (profile-driven FlashAttention-2 page):
+//  - "Where the last article left off": tiles of query rows, a loop over key
+//    tiles, running max m, running sum l and unnormalised O kept in fp32;
+//  - "Round 4 / exp2": raw scores S = Q K^T, m kept in log2 units of the scaled
+//    scores, P = 2^(S*qk_scale - m), alpha = 2^(m_old - m_new), and at the end
+//    O / l and L = (m + log2 l) ln 2 with qk_scale = scale * log2(e) > 0;
+//  - "Round 4 / Causal tile-skipping": key tiles past the diagonal are never
+//    visited; only the diagonal tile and a ragged last tile are masked
+//    (k_pos < N and, when causal, k_pos <= q_pos);
+//  - "Round 4 / The P cast": l sums the fp32 P; P is rounded to the input dtype
+//    for the second product.
+//
+// GB300 design (differs from the pages' Triton/Ada kernels):
+//  - one CTA owns 2 x 128 query rows of one (b, h). Each 128-row Q tile has one
+//    softmax warpgroup; one thread owns one query row, i.e. one TMEM lane, so the
+//    row max and row sum need no cross-thread reduction at all;
+//  - one TMA warp streams 128-key K and V tiles into a multi-stage shared-memory
+//    ring (128-byte swizzle); one thread issues every tcgen05.mma:
+//      S_t = Q_t K_j^T   (SMEM x SMEM -> TMEM fp32, 128 x 128)
+//      O_t += P_t V_j    (P from TMEM, 16-bit, aliasing S_t; V MN-major in SMEM)
+//    interleaved as S_0(j), PV_1(j-1), S_1(j), PV_0(j) so that the tensor core
+//    works on one Q tile while the other tile's softmax runs;
+//  - rescaling of O is lazy: a row keeps a stale maximum until the new maximum
+//    exceeds it by more than kRescaleTau (log2 units). P then stays <= 2^tau,
+//    and the result is unchanged because O and l share the stale maximum;
+//  - every mbarrier wait is bounded by a timer; on expiry the kernel records an
+//    error, stops issuing work, drains its copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn_sm103 {
+
+constexpr uint64_t kWaitTimeoutNs = 1500ull * 1000ull * 1000ull;  // 1.5 s
+constexpr float kRescaleTau = 8.0f;                                // log2 units
+constexpr uint32_t kErrTimeout = 1u;
+
+// Roles, for the error record.
+enum : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax0 = 3, kRoleSoftmax1 = 4 };
+
+template <int D>
+struct FwdCfg {
+    static_assert(D == 64 || D == 128, "head dimension must be 64 or 128");
+    static constexpr int BM = 128;  // query rows per Q tile = TMEM lanes
+    static constexpr int BN = 128;  // keys per K/V tile
+    static constexpr int kQTiles = 2;
+    static constexpr int kRowsPerCta = BM * kQTiles;
+    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 elements x 2 B
+    static constexpr int kChunks = D / 64;       // boxes per 128-row tile
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    // barriers: q_full[2] k_full[S] v_full[S] kv_empty[S] s_full[2] p_full[2] o_done[2] drain
+    static constexpr int kBarQFull = 0;
+    static constexpr int kBarKFull = 2;
+    static constexpr int kBarVFull = kBarKFull + kStages;
+    static constexpr int kBarKvEmpty = kBarVFull + kStages;
+    static constexpr int kBarSFull = kBarKvEmpty + kStages;
+    static constexpr int kBarPFull = kBarSFull + 2;
+    static constexpr int kBarODone = kBarPFull + 2;
+    static constexpr int kBarDrain = kBarODone + 2;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
+    // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D)
+    __device__ static constexpr uint32_t colS(int t) { return 128u * t; }
+    __device__ static constexpr uint32_t colO(int t) { return 256u + D * t; }
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kThreads = 320;  // warps 0-3 softmax 0, 4-7 softmax 1, 8 MMA, 9 TMA
+    static constexpr int kWarpMma = 8;
+    static constexpr int kWarpLoad = 9;
+};
+
+// Bounded wait state shared by all roles of one CTA.
+struct WaitCtx {
+    uint32_t* err;
+    volatile uint32_t* abort;  // shared memory: set once any role of this CTA gave up
+    uint32_t block;
+};
+
+static __device__ __noinline__ void record_timeout(const WaitCtx& w, uint32_t where, uint32_t iter) {
+    if (atomicCAS(w.err, 0u, kErrTimeout) == 0u) {
+        w.err[1] = w.block;
+        w.err[2] = where;
+        w.err[3] = iter;
+        __threadfence();
+    }
+    *w.abort = 1u;
+}
+
+// Single-thread bounded wait. With honor_abort, gives up as soon as another role of
+// the CTA has given up; without it (draining), waits for the phase up to the timeout.
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                       uint32_t where, uint32_t iter, bool honor_abort) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 0;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 63u) {
+            if (honor_abort && *w.abort) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                record_timeout(w, where, iter);
+                return false;
+            }
+        }
+    }
+}
+
+static __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                         uint32_t where, uint32_t iter, bool honor_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, w, where, iter, honor_abort);
+}
+
+// Whole-warp bounded wait: every lane observes the phase; lane 0 decides when to
+// give up so that the outcome is warp-uniform.
+static __device__ __noinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                            uint32_t where, uint32_t iter) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 0;; ++n) {
+        const bool done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        if ((n & 63u) == 63u) {
+            uint32_t give_up = 0;
+            if (lane == 0) {
+                if (*w.abort) give_up = 1;
+                else if (global_timer_ns() - t0 > kWaitTimeoutNs) give_up = 2;
+            }
+            give_up = __shfl_sync(0xffffffffu, give_up, 0);
+            if (give_up) {
+                if (lane == 0 && give_up == 2) record_timeout(w, where, iter);
+                return false;
+            }
+        }
+    }
+}
+
+static __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                          uint32_t where, uint32_t iter) {
+    const bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    return wait_warp_slow(bar, parity, w, where, iter);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const FwdParams p) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31u;
+
+    auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * i; };
+    auto sQ = [&](int t) -> uint32_t { return base + C::kOffQ + t * C::kTileBytes; };
+    auto sK = [&](int s) -> uint32_t { return base + C::kOffK + s * C::kTileBytes; };
+    auto sV = [&](int s) -> uint32_t { return base + C::kOffV + s * C::kTileBytes; };
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);  // [0] tmem base, [1] abort
+
+    // ---- which rows this CTA owns (heaviest causal tiles are launched first) --------
+    const int bh = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.BH));
+    const int ct = p.n_ctiles - 1 - static_cast<int>(blockIdx.x / static_cast<uint32_t>(p.BH));
+    const int N = p.N;
+    const int n_kv_all = (N + C::BN - 1) / C::BN;
+    int row0[2], n_kv[2];
+    for (int t = 0; t < 2; ++t) {
+        row0[t] = ct * C::kRowsPerCta + t * C::BM;
+        const bool valid = row0[t] < N;
+        int n = n_kv_all;
+        if (CAUSAL) n = min(n_kv_all, row0[t] / C::BN + 1);
+        n_kv[t] = valid ? n : 0;
+    }
+    const int n_max = max(n_kv[0], n_kv[1]);
+
+    WaitCtx wc{p.err, misc + 1, blockIdx.x};
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == C::kBarPFull || i == C::kBarPFull + 1) count = 128;
+            mbar_init(bar(i), count);
+        }
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == C::kWarpMma) {
+        tmem_alloc(smem_addr(misc), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    if (warp == C::kWarpLoad) {
+        // ================================ TMA producer ================================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_last();
+            for (int t = 0; t < 2; ++t) {
+                if (n_kv[t] == 0) continue;
+                mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d_hint(sQ(t) + c * C::kBoxBytes, &tmQ, bar(C::kBarQFull + t), c * 64,
+                                     row0[t], bh, pol_q);
+            }
+            int issued = 0;
+            for (int j = 0; j < n_max; ++j) {
+                const int s = j % C::kStages;
+                if (j >= C::kStages &&
+                    !wait_one(bar(C::kBarKvEmpty + s), ((j / C::kStages) - 1) & 1, wc,
+                              kRoleLoad * 1000 + C::kBarKvEmpty + s, j))
+                    break;
+                mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d_hint(sK(s) + c * C::kBoxBytes, &tmK, bar(C::kBarKFull + s), c * 64,
+                                     j * C::BN, bh, pol_kv);
+                mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d_hint(sV(s) + c * C::kBoxBytes, &tmV, bar(C::kBarVFull + s), c * 64,
+                                     j * C::BN, bh, pol_kv);
+                issued = j + 1;
+            }
+            // Drain: every copy issued into this CTA's shared memory has landed before
+            // the CTA can exit (on the normal path these phases completed long ago).
+            for (int t = 0; t < 2; ++t)
+                if (n_kv[t] > 0) wait_one(bar(C::kBarQFull + t), 0, wc, kRoleLoad * 1000 + 90 + t, 0, false);
+            for (int jj = max(0, issued - C::kStages); jj < issued; ++jj) {
+                const int s = jj % C::kStages;
+                const uint32_t ph = (jj / C::kStages) & 1;
+                wait_one(bar(C::kBarKFull + s), ph, wc, kRoleLoad * 1000 + 80, jj, false);
+                wait_one(bar(C::kBarVFull + s), ph, wc, kRoleLoad * 1000 + 81, jj, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::kWarpMma) {
+        // ================================ MMA issuer ==================================
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, 128, 128, false);
+            constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, 128, D, true);
+            bool ok = true;
+            for (int t = 0; t < 2 && ok; ++t)
+                if (n_kv[t] > 0)
+                    ok = wait_one(bar(C::kBarQFull + t), 0, wc, kRoleMma * 1000 + C::kBarQFull + t, 0);
+            tc_fence_after_sync();
+
+            auto issue_s = [&](int t, int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+                    const uint64_t a = sdesc_sw128(sQ(t) + off, 16, 1024);
+                    const uint64_t b = sdesc_sw128(sK(s) + off, 16, 1024);
+                    mma_f16_ss(tmem + C::colS(t), a, b, idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) {
+                    const uint64_t b = sdesc_sw128(sV(s) + kk * 2048, C::kBoxBytes, 1024);
+                    mma_f16_ts(tmem + C::colO(t), tmem + C::colS(t) + kk * 8, b, idesc_o,
+                               (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            for (int j = 0; j < n_max && ok; ++j) {
+                const int s = j % C::kStages;
+                const uint32_t ph = (j / C::kStages) & 1;
+                if (!wait_one(bar(C::kBarKFull + s), ph, wc, kRoleMma * 1000 + C::kBarKFull + s, j)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                if (j < n_kv[0]) {
+                    issue_s(0, s);
+                    mma_commit(bar(C::kBarSFull + 0));
+                }
+                if (j >= 1 && j - 1 < n_kv[1]) {
+                    if (!wait_one(bar(C::kBarPFull + 1), (j - 1) & 1, wc, kRoleMma * 1000 + C::kBarPFull + 1, j)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_pv(1, (j - 1) % C::kStages, j - 1 > 0);
+                    mma_commit(bar(C::kBarODone + 1));
+                }
+                if (j >= 1) mma_commit(bar(C::kBarKvEmpty + (j - 1) % C::kStages));
+                if (j < n_kv[1]) {
+                    issue_s(1, s);
+                    mma_commit(bar(C::kBarSFull + 1));
+                }
+                if (!wait_one(bar(C::kBarVFull + s), ph, wc, kRoleMma * 1000 + C::kBarVFull + s, j)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                if (j < n_kv[0]) {
+                    if (!wait_one(bar(C::kBarPFull + 0), j & 1, wc, kRoleMma * 1000 + C::kBarPFull, j)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_pv(0, s, j > 0);
+                    mma_commit(bar(C::kBarODone + 0));
+                }
+            }
+            if (ok && n_max >= 1 && n_max - 1 < n_kv[1]) {
+                const int j = n_max;
+                if (wait_one(bar(C::kBarPFull + 1), (j - 1) & 1, wc, kRoleMma * 1000 + C::kBarPFull + 1, j)) {
+                    tc_fence_after_sync();
+                    issue_pv(1, (j - 1) % C::kStages, j - 1 > 0);
+                    mma_commit(bar(C::kBarODone + 1));
+                }
+            }
+            // Drain: all MMAs issued by this thread are complete before TMEM is freed.
+            mma_commit(bar(C::kBarDrain));
+            wait_one(bar(C::kBarDrain), 0, wc, kRoleMma * 1000 + C::kBarDrain, 0, false);
+        }
+        __syncwarp();
+    } else {
+        // ================================ softmax warpgroups ==========================
+        const int t = static_cast<int>(warp >> 2);
+        const uint32_t wq = warp & 3u;            // TMEM lane quarter of this warp
+        const uint32_t r = wq * 32u + lane;       // row inside the Q tile = TMEM lane
+        const int q_row = row0[t] + static_cast<int>(r);
+        const uint32_t role = t == 0 ? kRoleSoftmax0 : kRoleSoftmax1;
+        const uint32_t tS = tmem_addr(tmem, wq * 32u, C::colS(t));
+        const uint32_t tO = tmem_addr(tmem, wq * 32u, C::colO(t));
+        const float qk = p.qk_scale;
+
+        bool ok = n_kv[t] > 0;
+        float m = -INFINITY;  // running max, log2 units of the scaled scores (possibly stale)
+        float l = 0.f;        // running sum of P (fp32), relative to m
+        for (int j = 0; j < n_kv[t] && ok; ++j) {
+            if (!wait_warp(bar(C::kBarSFull + t), j & 1, wc, role * 1000 + C::kBarSFull + t, j)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+
+            const int k0 = j * C::BN;
+            const bool need_mask = (k0 + C::BN > N) || (CAUSAL && k0 + C::BN - 1 > row0[t]);
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int kp = k0 + c * 32 + e;
+                        const bool keep = kp < N && (!CAUSAL || kp <= q_row);
+                        if (!keep) sr[c][e] = __float_as_uint(-INFINITY);
+                    }
+            }
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i >> 1][(i & 1) * 16]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int i = (c * 2 + (e >> 4)) & 7;
+                    mx[i] = fmaxf(mx[i], __uint_as_float(sr[c][e]));
+                }
+            const float row_max =
+                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            float m_new = fmaxf(m, row_max * qk);
+            if (m_new - m <= kRescaleTau) m_new = m;  // keep the stale max (false when m = -inf)
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            // rescale factor of the old state; exactly 1 when the maximum is kept
+            const float alpha = (m == m_use) ? 1.f : ex2_ftz(m - m_use);
+
+            uint32_t pk[2][32];
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const float x0 = __uint_as_float(sr[(2 * i) >> 5][(2 * i) & 31]);
+                const float x1 = __uint_as_float(sr[(2 * i + 1) >> 5][(2 * i + 1) & 31]);
+                const float p0 = ex2_ftz(fmaf(x0, qk, -m_use));
+                const float p1 = ex2_ftz(fmaf(x1, qk, -m_use));
+                sum[i & 3] += p0 + p1;
+                pk[i >> 5][i & 31] = pack2<BF16>(p0, p1);
+            }
+            l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+            tmem_st32(tS, pk[0]);
+            tmem_st32(tS + 32, pk[1]);
+            tmem_st_wait();
+
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O still holds the sum up to tile j-1 scaled by the old max.
+                if (!wait_warp(bar(C::kBarODone + t), (j - 1) & 1, wc, role * 1000 + C::kBarODone + t, j)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + c * 32, o);
+                }
+                tmem_st_wait();
+            }
+            m = m_new;
+            tc_fence_before_sync();
+            mbar_arrive(bar(C::kBarPFull + t));
+        }
+
+        // ---- epilogue: O / l -> dtype -> swizzled SMEM (reusing this Q tile) -> TMA store
+        if (ok) {
+            ok = wait_warp(bar(C::kBarODone + t), (n_kv[t] - 1) & 1, wc, role * 1000 + 70, n_kv[t]);
+        }
+        if (ok) {
+            tc_fence_after_sync();
+            const float inv_l = 1.f / l;
+            uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_ld_wait();
+                reg_fence(o);
+                uint32_t h[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    h[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+                const int box = c >> 1;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t chunk = (c & 1) * 4 + i;
+                    uint4 v = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                    *reinterpret_cast<uint4*>(stage + box * C::kBoxBytes + sw128_offset(r, chunk)) = v;
+                }
+            }
+            if (q_row < N) {
+                const float m_fin = (m == -INFINITY) ? 0.f : m;
+                p.lse[static_cast<size_t>(bh) * N + q_row] = (m_fin + log2f(l)) * 0.69314718055994530942f;
+            }
+        }
+        fence_proxy_async_smem();
+        if (n_kv[t] > 0) named_bar_sync(1 + t, 128);
+        if (n_kv[t] > 0 && wq == 0 && lane == 0 && *wc.abort == 0u) {
+            tma_prefetch_desc(&tmO);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_store_3d(&tmO, sQ(t) + c * C::kBoxBytes, c * 64, row0[t], bh);
+            tma_store_commit();
+            tma_store_wait_all();
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == C::kWarpMma) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace attn_sm103

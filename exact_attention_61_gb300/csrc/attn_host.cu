@@ -1,0 +1,242 @@
+// C ABI of the attention forward (see include/attn.h): argument validation,
+// tensor-map encoding, device status record and dispatch to the kernel instances.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+
+namespace attn_sm103 {
+
+thread_local int g_last_cuda_error = 0;
+
+// Device status record written by the kernels when a bounded wait gives up:
+// {status bits, linear block index, role*1000 + barrier id, loop iteration}.
+__device__ uint32_t g_status[4];
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return ATTN_ERR_CUDA;
+}
+
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (f) return f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
+        *err = e != cudaSuccess ? e : cudaErrorSymbolNotFound;
+        return nullptr;
+    }
+    f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    fn.store(f, std::memory_order_release);
+    return f;
+}
+
+// Device address of g_status on the current device (cached per device).
+uint32_t* status_ptr(int dev, cudaError_t* err) {
+    static std::atomic<uintptr_t> cache[64];
+    if (dev >= 0 && dev < 64) {
+        uintptr_t v = cache[dev].load(std::memory_order_acquire);
+        if (v) return reinterpret_cast<uint32_t*>(v);
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_status);
+    if (e != cudaSuccess) {
+        *err = e;
+        return nullptr;
+    }
+    if (dev >= 0 && dev < 64) cache[dev].store(reinterpret_cast<uintptr_t>(p), std::memory_order_release);
+    return static_cast<uint32_t*>(p);
+}
+
+namespace {
+
+bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    const uintptr_t ptrs[5] = {reinterpret_cast<uintptr_t>(q), reinterpret_cast<uintptr_t>(k),
+                               reinterpret_cast<uintptr_t>(v), reinterpret_cast<uintptr_t>(o),
+                               reinterpret_cast<uintptr_t>(lse)};
+    for (uintptr_t p : ptrs)
+        if (p % 16u) return ATTN_ERR_MISALIGNED;
+    const int64_t lim31 = (int64_t(1) << 31) - 1;
+    if (B > lim31 || H > lim31 || N > lim31) return ATTN_ERR_UNSUPPORTED;
+    if (B * H > lim31) return ATTN_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    if (BH > (int64_t(1) << 62) / (N * d)) return ATTN_ERR_UNSUPPORTED;
+    const int64_t n_ctiles = (N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
+    if (n_ctiles * BH > lim31) return ATTN_ERR_UNSUPPORTED;
+    const uint64_t tensor_bytes = static_cast<uint64_t>(BH * N * d) * 2u;
+    const uint64_t lse_bytes = static_cast<uint64_t>(BH * N) * 4u;
+    if (ranges_overlap(o, tensor_bytes, q, tensor_bytes) ||
+        ranges_overlap(o, tensor_bytes, k, tensor_bytes) ||
+        ranges_overlap(o, tensor_bytes, v, tensor_bytes) ||
+        ranges_overlap(o, tensor_bytes, lse, lse_bytes) ||
+        ranges_overlap(lse, lse_bytes, q, tensor_bytes) ||
+        ranges_overlap(lse, lse_bytes, k, tensor_bytes) ||
+        ranges_overlap(lse, lse_bytes, v, tensor_bytes))
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+// 3-D tensor map over a contiguous [BH][N][d] 16-bit array: box 64 x 128 x 1,
+// 128-byte swizzle, out-of-range rows read as zero and are not written.
+CUresult make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* ptr,
+                  int64_t BH, int64_t N, int64_t d, int dtype) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(N * d * 2)};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+               3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// Make the device that owns `ptr` current for this runtime instance.
+cudaError_t select_device_of(const void* ptr, int* dev_out) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+    if (e != cudaSuccess) return e;
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return cudaErrorInvalidDevicePointer;
+    int cur = -1;
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    if (cur != attr.device) {
+        e = cudaSetDevice(attr.device);
+        if (e != cudaSuccess) return e;
+    }
+    *dev_out = attr.device;
+    return cudaSuccess;
+}
+
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+             int64_t N, int64_t d, int causal, float scale, int dtype, void* stream, uint32_t** status_out) {
+    const int st = validate(q, k, v, o, lse, B, H, N, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    cudaError_t e = select_device_of(q, &dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaSuccess;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn(&e);
+    if (!enc) return cuda_fail(e);
+    uint32_t* status = status_ptr(dev, &e);
+    if (!status) return cuda_fail(e);
+    if (status_out) *status_out = status;
+
+    const int64_t BH = B * H;
+    alignas(64) CUtensorMap maps[4];
+    const void* ptrs[4] = {q, k, v, o};
+    for (int i = 0; i < 4; ++i) {
+        const CUresult r = make_map(enc, &maps[i], ptrs[i], BH, N, d, dtype);
+        if (r != CUDA_SUCCESS) {
+            g_last_cuda_error = 100000 + static_cast<int>(r);
+            return ATTN_ERR_CUDA;
+        }
+    }
+    FwdParams p;
+    p.lse = lse;
+    p.err = status;
+    p.N = static_cast<int>(N);
+    p.BH = static_cast<int>(BH);
+    p.n_ctiles = static_cast<int>((N + kFwdRowsPerCta - 1) / kFwdRowsPerCta);
+    p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool c = causal != 0;
+    if (d == 64)
+        e = dtype == ATTN_BF16 ? launch_fwd_d64_bf16(c, maps, p, s) : launch_fwd_d64_f16(c, maps, p, s);
+    else
+        e = dtype == ATTN_BF16 ? launch_fwd_d128_bf16(c, maps, p, s) : launch_fwd_d128_f16(c, maps, p, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn_sm103
+
+using namespace attn_sm103;
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+             int64_t N, int64_t d, int causal, float scale, int dtype, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream, nullptr);
+}
+
+int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                     int64_t H, int64_t N, int64_t d, int causal, float scale, int dtype, void* stream) {
+    int st = validate(q, k, v, o, lse, B, H, N, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    cudaError_t e = select_device_of(q, &dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t* status = status_ptr(dev, &e);
+    if (!status) return cuda_fail(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream, nullptr);
+    if (st != ATTN_OK) return st;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t host[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(host, status, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return host[0] ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+const char* attn_strerror(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, size < 1, bad scale or dtype, or overlapping outputs)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dimension must be 64 or 128; sizes within the documented limits)";
+        case ATTN_ERR_MISALIGNED: return "misaligned pointer (all tensors must be 16-byte aligned)";
+        case ATTN_ERR_CUDA: return "CUDA error (see attn_last_cuda_error)";
+        case ATTN_ERR_TIMEOUT: return "device-side wait timed out (outputs undefined)";
+        default: return "unknown status";
+    }
+}
+
+int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int attn_device_error_info(int32_t info[4]) {
+    if (!info) return ATTN_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t* status = status_ptr(dev, &e);
+    if (!status) return cuda_fail(e);
+    uint32_t host[4];
+    e = cudaMemcpy(host, status, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (int i = 0; i < 4; ++i) info[i] = static_cast<int32_t>(host[i]);
+    return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+/*
+ * attn.h -- C ABI of the fused exact scaled-dot-product attention forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (plain definition, per head and query row i):
+ *
+ *     O[i,:]  = sum_{j in V_i} softmax_j(scale * q_i . k_j) * v_j
+ *     LSE[i]  = ln sum_{j in V_i} exp(scale * q_i . k_j)
+ *     V_i     = { 0 <= j < N }, or { 0 <= j <= i } under the causal mask
+ *
+ * Sources for the operation and its argument list:
+ *  - "Programming an attention kernel in Triton", Kernel 4 (a self-attention
+ *    kernel): scores = scale * Q K^T, masked keys set to -inf, row softmax,
+ *    weights times V.
+ *  - "如何用 profiler 逐步优化 Triton FlashAttention-2 kernel" (profile-driven
+ *    FlashAttention-2 page), "What the compiler did": the kernel takes
+ *    Q, K, V, O, L, the sequence lengths, the scale, the head dimension D and
+ *    is_causal; "Round 4 / Causal tile-skipping" fixes the mask as
+ *    k_pos <= q_pos (top-left aligned); "Round 4 / exp2" fixes L as the
+ *    natural-log logsumexp of the scaled scores.
+ *  - "如何用 profiler ...", "A small program to profile": Q, K, V, O are stored
+ *    as contiguous (B*H, N, D) blocks and viewed as (B, H, N, D).
+ *
+ * Conventions shared by every call below:
+ *  - q, k, v, o: DEVICE pointers to contiguous row-major [B, H, N, d] arrays of
+ *    `dtype` (fp16 or bf16). lse: DEVICE pointer to a contiguous [B, H, N] fp32
+ *    array. All five must be 16-byte aligned. o and lse must not overlap each
+ *    other or the inputs. The inputs are only read.
+ *  - The caller owns and allocates all device memory. The library allocates no
+ *    device memory; it keeps a few host-side caches (function attributes and
+ *    the driver entry point) that are set up on first use.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). The call is
+ *    asynchronous on that stream; argument errors are reported synchronously,
+ *    before anything is enqueued.
+ *  - Supported: d in {64, 128}; B, H, N >= 1; B*H < 2^31; N < 2^31;
+ *    B*H*N*d < 2^62; scale finite and > 0 (the kernel folds scale*log2(e)
+ *    into one positive factor applied after the row maximum, which needs a
+ *    positive scale). Anything else is rejected; there is no fallback path.
+ *  - Thread-safe: concurrent calls on different streams are allowed.
+ *  - Accumulation is fp32; O is rounded once to `dtype` (round to nearest even).
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_FP16 = 0,
+    ATTN_BF16 = 1
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, size < 1, bad scale or dtype, overlap   */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not built: d not in {64,128}, sizes too big */
+    ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned                        */
+    ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed; see
+                                  attn_last_cuda_error()                                  */
+    ATTN_ERR_TIMEOUT = 5       /* a device-side wait ran out (attn_fwd_checked only); the
+                                  outputs are undefined and the context stays usable      */
+} attn_status_t;
+
+/*
+ * attn_fwd -- enqueue the forward pass on `stream`.
+ *
+ * Computes o = softmax(scale * q k^T [+ causal mask]) v and lse (natural log)
+ * for every (b, h) and query row, as defined at the top of this header.
+ * causal != 0 selects the top-left mask j <= i. dtype is an attn_dtype_t.
+ * Returns ATTN_OK once the kernel is enqueued, or an error status with nothing
+ * enqueued. Device-side faults surface at the caller's next synchronisation.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+             int dtype, void* stream);
+
+/*
+ * attn_fwd_checked -- attn_fwd, then synchronise `stream` and read the device
+ * status word. Returns ATTN_ERR_TIMEOUT if any device-side wait gave up (the
+ * kernel bounds every wait instead of spinning forever), ATTN_ERR_CUDA if the
+ * launch or the synchronisation failed, else ATTN_OK. Meant for tests and
+ * debugging: it blocks the calling host thread. It clears the device status
+ * word before the launch, so concurrent checked calls on different streams
+ * may see each other's status.
+ */
+int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                     int dtype, void* stream);
+
+/* attn_strerror -- static, human-readable text for an attn_status_t. Never NULL. */
+const char* attn_strerror(int status);
+
+/* attn_last_cuda_error -- the cudaError_t behind the last ATTN_ERR_CUDA returned
+ * on the calling host thread (0 if none). */
+int attn_last_cuda_error(void);
+
+/*
+ * attn_device_error_info -- copy the device status record into info[0..3]:
+ * {status bits, linear block index, role*1000 + barrier id, loop iteration}
+ * of the first wait that gave up since the record was last cleared (all zero if
+ * none). Synchronous (reads device memory of the current device). Returns
+ * ATTN_OK or ATTN_ERR_CUDA; ATTN_ERR_INVALID_ARG if info is NULL. Diagnostics
+ * only; the pages have no counterpart.
+ */
+int attn_device_error_info(int32_t info[4]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

@@ -1,0 +1,41 @@
+/*
+ * attn_probe.h -- test hook that runs the two tensor-core products of the
+ * attention forward on one 128-row tile, through exactly the TMA, shared-memory
+ * descriptor, tcgen05 and TMEM forms the forward kernel uses.
+ *
+ * The products are the two contractions of the FlashAttention-2 inner loop
+ * ("如何用 profiler 逐步优化 Triton FlashAttention-2 kernel", Round 4 / exp2:
+ * S_ij = Q_i K_j^T on raw scores; Round 4 / The P cast: P rounded to the input
+ * dtype, then P V_j on the 16-bit tensor-core path).
+ *
+ * It exists so that descriptor or layout mistakes show up as a wrong number on
+ * one tile rather than as a wrong attention output. Not part of the product API.
+ */
+#ifndef ATTN_GB300_ATTN_PROBE_H
+#define ATTN_GB300_ATTN_PROBE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * attn_probe_tile -- one CTA, synchronous on `stream` (it synchronises before
+ * returning).
+ *  q, k, v : DEVICE, contiguous row-major [128][d] of `dtype` (attn_dtype_t).
+ *  p       : DEVICE, contiguous row-major [128][128] of `dtype`.
+ *  s_out   : DEVICE, [128][128] fp32, receives S = q k^T   (tcgen05, SMEM x SMEM).
+ *  o_out   : DEVICE, [128][d]   fp32, receives O = p v     (tcgen05, P from TMEM,
+ *            V as an MN-major shared-memory operand).
+ *  d in {64, 128}. All pointers 16-byte aligned.
+ * Returns an attn_status_t (ATTN_ERR_TIMEOUT if a device wait gave up).
+ */
+int attn_probe_tile(const void* q, const void* k, const void* v, const void* p, float* s_out,
+                    float* o_out, int64_t d, int dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_PROBE_H */

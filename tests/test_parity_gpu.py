@@ -1,0 +1,163 @@
+"""Parity of the CUDA forward (through the C ABI) with the fp64 CPU oracle.
+
+Tolerances (max-abs, per element): O within 4e-3 for fp16 and 3.2e-2 for bf16;
+LSE within 1e-3. Small problems are compared element by element in full; the
+large ones (every row of which the oracle would need minutes for) are compared
+on sampled rows computed one by one by the oracle, plus properties that hold at
+any size (causal row 0 equals V[0] exactly, outputs finite and inside the range
+of V, determinism).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gen import WORKLOADS, make_qkv, sweep_points, workload
+
+TOL_O = {"fp16": 4e-3, "bf16": 3.2e-2}
+TOL_LSE = 1e-3
+
+
+def _run(attn, q, k, v, causal, scale):
+    o, lse = attn.fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, checked=True)
+    return o.cpu(), lse.cpu()
+
+
+def _report(name, o_gpu, lse_gpu, o_ref, lse_ref, dtype):
+    o64 = o_gpu.to(torch.float64).numpy().reshape(o_ref.shape)
+    l64 = lse_gpu.to(torch.float64).numpy().reshape(lse_ref.shape)
+    assert np.isfinite(o64).all() and np.isfinite(l64).all(), f"{name}: non-finite output"
+    eo = np.abs(o64 - o_ref)
+    el = np.abs(l64 - lse_ref)
+    tol = TOL_O[dtype]
+    msg = (f"{name}: max|dO| = {eo.max():.3e} (tol {tol}, {int((eo > tol).sum())} over), "
+           f"max|dLSE| = {el.max():.3e} (tol {TOL_LSE}, {int((el > TOL_LSE).sum())} over)")
+    assert eo.max() <= tol and el.max() <= TOL_LSE, msg
+    return eo.max(), el.max()
+
+
+def _full(attn, B, H, N, d, dtype, causal, seed, input_scale=1.0):
+    q, k, v = make_qkv(B, H, N, d, dtype, seed, input_scale)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(attn, q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    return _report(f"B{B}H{H}N{N}d{d}{dtype}{'c' if causal else ''}", o, lse, o_ref, lse_ref, dtype)
+
+
+def _sample_rows(BH, N, rng, heads=16, per_head=12):
+    hs = np.unique(np.linspace(0, BH - 1, min(BH, heads)).astype(np.int64))
+    fixed = [0, 1, 2, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    rows = []
+    for h in hs:
+        r = [x for x in fixed if 0 <= x < N] + list(rng.integers(0, N, size=per_head))
+        rows.extend(int(h) * N + x for x in sorted(set(r)))
+    return np.array(rows, dtype=np.int64)
+
+
+def _sampled(attn, B, H, N, d, dtype, causal, seed, input_scale=1.0):
+    q, k, v = make_qkv(B, H, N, d, dtype, seed, input_scale)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(attn, q, k, v, causal, scale)
+    rows = _sample_rows(B * H, N, np.random.default_rng(seed))
+    o_ref, lse_ref = oracle.attn_fwd_rows(q, k, v, causal, rows, scale)
+    og = o.reshape(-1, d)[torch.from_numpy(rows)]
+    lg = lse.reshape(-1)[torch.from_numpy(rows)]
+    name = f"B{B}H{H}N{N}d{d}{dtype}{'c' if causal else ''}x{input_scale:g}"
+    _report(name, og, lg, o_ref, lse_ref, dtype)
+    # properties over every output
+    of = o.to(torch.float32)
+    assert torch.isfinite(of).all() and torch.isfinite(lse).all(), f"{name}: non-finite"
+    vf = v.to(torch.float32)
+    vmax = vf.amax(dim=2, keepdim=True)
+    vmin = vf.amin(dim=2, keepdim=True)
+    tol = TOL_O[dtype]
+    assert (of <= vmax + tol).all() and (of >= vmin - tol).all(), f"{name}: O outside range of V"
+    if causal:
+        assert torch.equal(o[:, :, 0], v[:, :, 0]), f"{name}: causal row 0 differs from V[0]"
+    return o, lse
+
+
+# ---- the named workloads ------------------------------------------------------------------
+
+@pytest.mark.gpu
+def test_smallest(cuda_lib):
+    w = workload("b1h1n128d64")
+    _full(cuda_lib, w.B, w.H, w.N, w.d, "fp16", False, w.seed)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_boundary_n1000(cuda_lib, dtype, causal):
+    w = workload("b2h4n1000d64")
+    _full(cuda_lib, w.B, w.H, w.N, w.d, dtype, causal, w.seed)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_headline_b4h16n4096d64(cuda_lib, causal):
+    w = workload("b4h16n4096d64")
+    _sampled(cuda_lib, w.B, w.H, w.N, w.d, "bf16", causal, w.seed)
+
+
+@pytest.mark.gpu
+def test_long_b1h16n8192d128_scaled(cuda_lib):
+    w = workload("b1h16n8192d128x2")
+    _sampled(cuda_lib, w.B, w.H, w.N, w.d, "bf16", True, w.seed, w.input_scale)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("pt", list(sweep_points()),
+                         ids=lambda p: f"N{p['N']}d{p['d']}{p['dtype']}{'c' if p['causal'] else ''}")
+def test_sweep(cuda_lib, pt):
+    _sampled(cuda_lib, pt["B"], pt["H"], pt["N"], pt["d"], pt["dtype"], pt["causal"], pt["seed"])
+
+
+# ---- edge shapes: ragged tails, single key, one tile, tile +- 1 ------------------------------
+
+EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 384, 513]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N", EDGE_N)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_edge_shapes(cuda_lib, N, d, dtype, causal):
+    _full(cuda_lib, 1, 3, N, d, dtype, causal, seed=9000 + N * 4 + d)
+
+
+@pytest.mark.gpu
+def test_nondefault_scale_and_many_heads(cuda_lib):
+    q, k, v = make_qkv(3, 5, 300, 64, "bf16", seed=4242)
+    for causal in (False, True):
+        o, lse = _run(cuda_lib, q, k, v, causal, 0.37)
+        o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 0.37)
+        _report("scale0.37", o, lse, o_ref, lse_ref, "bf16")
+
+
+@pytest.mark.gpu
+def test_deterministic_and_unchecked_path(cuda_lib):
+    q, k, v = (t.cuda() for t in make_qkv(2, 4, 1000, 64, "bf16", seed=11))
+    for causal in (False, True):
+        o1, l1 = cuda_lib.fwd(q, k, v, causal=causal, checked=True)
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            o2, l2 = cuda_lib.fwd(q, k, v, causal=causal)
+        stream.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert cuda_lib.device_error_info() == [0, 0, 0, 0]
+
+
+@pytest.mark.gpu
+def test_rejects_bad_device_arguments(cuda_lib):
+    from exact_attention_61_gb300.attn import AttnError
+    q, k, v = (t.cuda() for t in make_qkv(1, 1, 64, 96, "bf16", seed=1))
+    with pytest.raises(AttnError) as e:
+        cuda_lib.fwd(q, k, v)
+    assert e.value.status == 2
+    q, k, v = (t.cuda() for t in make_qkv(1, 1, 64, 64, "bf16", seed=1))
+    with pytest.raises(AttnError):
+        cuda_lib.fwd(q, k, v, scale=-1.0)
