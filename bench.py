@@ -1,0 +1,456 @@
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one pass of the whole hot path over the B=4, H=16, N=4096, d=64 bf16
+problem: the non-causal forward and the causal forward (causal tile skipping is
+part of the path), each one launch of the sm_103a kernel through the C ABI.
+FLOPs per step = 4*B*H*N^2*d + (4*B*H*N^2*d)/2 (the causal half), the
+convention of the profile-driven FlashAttention-2 page (Round 0 / Step 5).
+
+Timing: W warm-up steps (plus enough extra steps to keep the GPU busy for
+--warmup-seconds, so clocks have ramped), peak-memory counters reset after
+warm-up, then K steps timed with CUDA events on the launching stream, the L2
+cache flushed (a write of twice its size) before every step outside the events,
+a barrier and a synchronize on both sides of the timed region, max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0. With --gpus N > 1 (under torchrun) every rank
+runs an independent replica of the same problem on its own GPU; nothing is
+exchanged on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s at B=4,H=16,N=4096,d=64 bf16; % of tensor-core peak"
+UNIT = "TFLOP/s"
+B, H, N, D = 4, 16, 4096, 64
+DTYPE = "bf16"
+SEED = 61002
+WORKLOAD = "b4h16n4096d64 bf16, non-causal + causal forward per step"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_b4h16n4096d64.md")
+KERNEL_SOURCES = ["exact_attention_61_gb300/csrc/attn_fwd_kernel.cuh",
+                  "exact_attention_61_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_61_gb300/csrc/attn_internal.h",
+                  "exact_attention_61_gb300/csrc/attn_fwd_inst.cu"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# pure host logic (tested on the CPU)
+# ---------------------------------------------------------------------------------------------
+
+def step_flops() -> float:
+    from exact_attention_61_gb300 import counts
+    return counts.attn_flops(B, H, N, D, False) + counts.attn_flops(B, H, N, D, True)
+
+
+def tflops(flops: float, ms: float) -> float:
+    return flops / (ms * 1e-3) / 1e12
+
+
+def aggregate(ms_per_rank, flops_per_rank_step: float, world: int) -> dict:
+    """Whole-job throughput: all ranks' work over the slowest rank's time."""
+    ms = max(ms_per_rank)
+    return {"ms_per_step": ms, "value": tflops(flops_per_rank_step * world, ms)}
+
+
+def allreduce_max(values, world: int, device=None):
+    """Element-wise maximum of `values` over all ranks (identity for one rank)."""
+    if world <= 1:
+        return [float(x) for x in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary_path: str = PROFILE_SUMMARY):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None if there is none or the kernel source changed since it was taken."""
+    if not os.path.exists(summary_path):
+        return None
+    text = open(summary_path).read()
+    mh = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    mt = re.search(r"dram_bytes_per_launch_noncausal:\s*([0-9]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_source_hash():
+        return None
+    return int(mt.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return {"bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "hbm_gbs": float(j.get("hbm_gbs", 6800.0)), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def summarize_clocks(samples, t0: float, t1: float) -> dict:
+    """Median SM clock and active throttle reasons over samples taken in [t0, t1]."""
+    win = [s for s in samples if t0 <= s["t"] <= t1]
+    if not win:
+        win = samples[-3:]
+    if not win:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    reasons = sorted({r for s in win for r in s["reasons"]})
+    return {"sm_mhz": statistics.median(s["sm"] for s in win),
+            "sm_max_mhz": max(s["sm_max"] for s in win),
+            "power_w_max": max(s["power"] for s in win),
+            "reasons": reasons, "samples": len(win)}
+
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.error = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.proc = None
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                self.samples.append({
+                    "t": time.time(), "sm": float(parts[0]), "sm_max": float(parts[1]),
+                    "power": float(parts[2]) if parts[2] not in ("[N/A]", "N/A") else 0.0,
+                    "reasons": [r for r, v in zip(self.REASONS, parts[3:]) if v == "Active"]})
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on the host cores, on a bounded sample of the workload
+# ---------------------------------------------------------------------------------------------
+
+def _sample_rows(n_rows: int, seed: int = 0):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, B * H * N, size=n_rows).astype(np.int64)
+
+
+def _row_flops(rows, causal: bool) -> float:
+    if not causal:
+        return 4.0 * N * D * len(rows)
+    return float(sum(4.0 * ((int(r) % N) + 1) * D for r in rows))
+
+
+def oracle_rate(q64, k64, v64, n_rows: int, seed: int = 0):
+    """Time the oracle on n_rows sampled query rows under each mask. Returns
+    (FLOPs, seconds)."""
+    import oracle
+    rows = _sample_rows(n_rows, seed)
+    scale = 1.0 / math.sqrt(D)
+    flops = secs = 0.0
+    for causal in (False, True):
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(q64, k64, v64, causal, rows, scale)
+        secs += time.perf_counter() - t0
+        flops += _row_flops(rows, causal)
+    return flops, secs
+
+
+def calibrate_rows(q64, k64, v64, target_s: float) -> int:
+    n = 64
+    while True:
+        _, s = oracle_rate(q64, k64, v64, n, seed=1)
+        if s >= 0.5 or n >= 1 << 20:
+            return max(16, int(n * target_s / max(s, 1e-6)))
+        n *= 4
+
+
+def cpu_baseline(q, k, v, target_s: float = 12.0) -> dict:
+    import oracle
+    q64, k64, v64 = oracle.to_f64(q), oracle.to_f64(k), oracle.to_f64(v)
+    n = calibrate_rows(q64, k64, v64, target_s)
+    flops, secs = oracle_rate(q64, k64, v64, n, seed=2)
+    return {"value": tflops(flops, secs * 1e3), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} random query rows of the B=4,H=16,N=4096,d=64 bf16 problem, "
+                      f"each under both masks, fp64 C oracle; {secs:.1f} s of CPU work"}
+
+
+# ---------------------------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------------------------
+
+def rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def run_reference(args) -> int:
+    rank, _, world = rank_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from gen import make_qkv
+    q, k, v = make_qkv(B, H, N, D, DTYPE, SEED)
+    q64, k64, v64 = oracle.to_f64(q), oracle.to_f64(k), oracle.to_f64(v)
+    n = calibrate_rows(q64, k64, v64, target_s=args.ref_step_seconds)
+    for i in range(max(args.warmup, 0)):
+        oracle_rate(q64, k64, v64, n, seed=100 + i)
+    total_f = total_s = 0.0
+    for i in range(args.steps):
+        f, s = oracle_rate(q64, k64, v64, n, seed=1000 + i)
+        total_f += f
+        total_s += s
+    value = tflops(total_f, total_s * 1e3)
+    ms = total_s * 1e3 / max(args.steps, 1)
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D,
+                      "step": f"{n} sampled query rows x both masks"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                            "kind": "oracle",
+                            "sample": f"{n} random query rows per step under both masks, fp64 C oracle"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def run_ours(args) -> int:
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_61_gb300 import attn, counts
+    from gen import make_qkv
+
+    rank, local_rank, world = rank_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device for --impl ours")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    attn.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    q_h, k_h, v_h = make_qkv(B, H, N, D, DTYPE, SEED)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(D)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    dt = attn.ATTN_BF16
+
+    def launch(causal):
+        st = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           B, H, N, D, causal, scale, dt, sptr)
+        if st != attn.ATTN_OK:
+            raise RuntimeError(f"attn_fwd failed: {attn.strerror(st)}")
+
+    sampler = ClockSampler(local_rank) if args.clocks else None
+    # ---- warm-up: W steps, then keep the GPU busy until --warmup-seconds have passed -----
+    t_w = time.perf_counter()
+    n_warm = 0
+    while n_warm < args.warmup or time.perf_counter() - t_w < args.warmup_seconds:
+        flush.fill_(n_warm & 0xFF)
+        launch(False)
+        launch(True)
+        n_warm += 1
+        if n_warm % 16 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+
+    # ---- timed region ------------------------------------------------------------------
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    w0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        launch(False)
+        ev[i][1].record(stream)
+        launch(True)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall_s = time.perf_counter() - w0
+    t1 = time.time()
+    launches = 2 * args.steps
+    t_nc = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    t_c = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    t_step = [a + b for a, b in zip(t_nc, t_c)]
+    ms_local = statistics.fmean(t_step)
+    peak_mem_gb = torch.cuda.max_memory_allocated(dev) / 1e9
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region) --
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    o_host = [torch.empty_like(qp).pin_memory() for _ in range(2)]
+    l_host = [torch.empty((B, H, N), dtype=torch.float32).pin_memory() for _ in range(2)]
+    e2e_steps = max(3, min(args.steps, 50))
+    h2d = 3 * q_h.numel() * q_h.element_size()
+    d2h = 2 * (o.numel() * o.element_size() + lse.numel() * 4)
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        for j, causal in enumerate((False, True)):
+            launch(causal)
+            o_host[j].copy_(o, non_blocking=True)
+            l_host[j].copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms_local = e_start.elapsed_time(e_end) / e2e_steps
+    if sampler:
+        sampler.stop()
+
+    # ---- aggregate over ranks -----------------------------------------------------------
+    ms, e2e_ms, ms_nc, ms_c = allreduce_max(
+        [ms_local, e2e_ms_local, statistics.fmean(t_nc), statistics.fmean(t_c)], world, dev)
+    if rank == 0:
+        peaks = measured_peaks()
+        f_nc = counts.attn_flops(B, H, N, D, False)
+        f_c = counts.attn_flops(B, H, N, D, True)
+        agg = aggregate([ms], f_nc + f_c, world)
+        achieved = tflops(f_nc, ms_nc)
+        traffic = profiled_traffic()
+        out = {
+            "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": n_warm, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "scale": scale,
+                       "causal": [False, True], "seed": SEED,
+                       "l2": "flushed before every step (write of 2x L2 size, outside the events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "per_kernel": {
+                "noncausal": {"ms_mean": ms_nc, "ms_median": statistics.median(t_nc),
+                              "ms_p10": _pct(t_nc, 10), "ms_p90": _pct(t_nc, 90),
+                              "tflops": tflops(f_nc, ms_nc), "frac_of_peak": tflops(f_nc, ms_nc) / peaks["bf16_tflops"]},
+                "causal": {"ms_mean": ms_c, "ms_median": statistics.median(t_c),
+                           "ms_p10": _pct(t_c, 10), "ms_p90": _pct(t_c, 90),
+                           "tflops": tflops(f_c, ms_c), "frac_of_peak": tflops(f_c, ms_c) / peaks["bf16_tflops"],
+                           "executed_tflops": tflops(counts.kernel_executed_flops(B, H, N, D, True), ms_c)}},
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<64,false,bf16>",
+                         "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                         "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
+                         if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16",
+                         "algorithmic_flops_per_launch": f_nc},
+            "e2e": {"value": tflops((f_nc + f_c) * world, e2e_ms), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "wall_s_timed_region": wall_s,
+            "peak_mem_gb": peak_mem_gb,
+        }
+        if sampler:
+            out["clocks"] = summarize_clocks(sampler.samples, t0 - args.warmup_seconds, t1)
+        if args.cpu_baseline and world == 1:
+            log("timing the fp64 oracle on the host cores ...")
+            out["cpu_baseline"] = cpu_baseline(q_h, k_h, v_h, target_s=args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _pct(xs, p):
+    s = sorted(xs)
+    return s[min(len(s) - 1, max(0, int(round(p / 100.0 * (len(s) - 1)))))]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--warmup-seconds", type=float, default=1.0,
+                    help="keep warming up until the GPU has been busy this long")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the oracle baseline")
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0,
+                    help="CPU work per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    return ap.parse_args(argv)
+
+
+def main(argv=None) -> int:
+    args = parse_args(argv)
+    if args.steps < 1:
+        raise SystemExit("--steps must be >= 1")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

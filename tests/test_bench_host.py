@@ -1,0 +1,109 @@
+"""Host logic of bench.py, on the CPU: throughput aggregation, the max-over-ranks
+reduction across two gloo ranks, clock summaries, the ncu-traffic bookkeeping and
+the reference (oracle) arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_step_flops_and_aggregate():
+    f = bench.step_flops()
+    assert f == pytest.approx(274.877906944e9 * 1.5)
+    a = bench.aggregate([0.4, 0.5], f, world=2)
+    assert a["ms_per_step"] == 0.5
+    assert a["value"] == pytest.approx(2 * f / 0.5e-3 / 1e12)
+
+
+def test_defaults_meet_the_timing_rules():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1 and a.impl == "ours"
+
+
+def test_clock_summary():
+    s = [{"t": 1.0, "sm": 1900, "sm_max": 2070, "power": 900, "reasons": []},
+         {"t": 2.0, "sm": 1800, "sm_max": 2070, "power": 1300, "reasons": ["sw_power_cap"]},
+         {"t": 3.0, "sm": 2000, "sm_max": 2070, "power": 1000, "reasons": []},
+         {"t": 9.0, "sm": 300, "sm_max": 2070, "power": 90, "reasons": []}]
+    c = bench.summarize_clocks(s, 0.5, 3.5)
+    assert c["sm_mhz"] == 1900 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"] and c["samples"] == 3
+
+
+def test_traffic_only_for_the_profiled_kernel(tmp_path):
+    p = tmp_path / "summary.md"
+    p.write_text(f"kernel_source_sha256: {bench.kernel_source_hash()}\n"
+                 "dram_bytes_per_launch_noncausal: 123456\n")
+    assert bench.profiled_traffic(str(p)) == 123456
+    p.write_text("kernel_source_sha256: 0000000000000000\ndram_bytes_per_launch_noncausal: 1\n")
+    assert bench.profiled_traffic(str(p)) is None
+    assert bench.profiled_traffic(str(tmp_path / "missing.md")) is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    vals = bench.allreduce_max([1.0 + rank, 5.0 - rank, 0.25 * (rank + 1)], world)
+    agg = bench.aggregate([vals[0]], 1e12, world)
+    q.put((rank, vals, agg))
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, vals, agg in out:
+        assert vals == [2.0, 5.0, 0.5]            # element-wise max over both ranks
+        assert agg["value"] == pytest.approx(2e12 / 2e-3 / 1e12)  # both ranks' work / slowest time
+
+
+def _run_bench(args, env_extra=None):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], env=env,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_json_line():
+    r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0",
+                    "--ref-step-seconds", "0.2"])
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in j
+    assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == "TFLOP/s"
+    assert j["value"] > 0 and j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["value"] == j["value"]
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
