@@ -55,7 +55,11 @@ struct FwdCfg {
     static constexpr int BN = 128;  // keys per K/V tile
     static constexpr int kQTiles = 2;
     static constexpr int kRowsPerCta = BM * kQTiles;
+    static_assert(kRowsPerCta == kFwdRowsPerCta, "host and kernel disagree on rows per CTA");
     static constexpr int kStages = D == 64 ? 4 : 2;
+    // S/P buffers in TMEM, rotated over the jobs of both Q tiles: with 3 buffers a
+    // tile's next S is computed while its softmax still runs.
+    static constexpr int kSBufs = D == 64 ? 3 : 2;
     static constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 elements x 2 B
     static constexpr int kChunks = D / 64;       // boxes per 128-row tile
     static constexpr int kTileBytes = 128 * D * 2;
@@ -63,25 +67,48 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-    // barriers: q_full[2] k_full[S] v_full[S] kv_empty[S] s_full[2] p_full[2] o_done[2] drain
+    // barriers: q_full[2] k_full[St] v_full[St] kv_empty[St] s_full[Sb] p_full[Sb] o_done[2] drain
     static constexpr int kBarQFull = 0;
     static constexpr int kBarKFull = 2;
     static constexpr int kBarVFull = kBarKFull + kStages;
     static constexpr int kBarKvEmpty = kBarVFull + kStages;
     static constexpr int kBarSFull = kBarKvEmpty + kStages;
-    static constexpr int kBarPFull = kBarSFull + 2;
-    static constexpr int kBarODone = kBarPFull + 2;
+    static constexpr int kBarPFull = kBarSFull + kSBufs;
+    static constexpr int kBarODone = kBarPFull + kSBufs;
     static constexpr int kBarDrain = kBarODone + 2;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
-    // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D)
-    __device__ static constexpr uint32_t colS(int t) { return 128u * t; }
-    __device__ static constexpr uint32_t colO(int t) { return 256u + D * t; }
+    // TMEM columns: S/P buffers [0, 128*kSBufs), then O_0 and O_1 (D columns each)
+    __device__ static constexpr uint32_t colS(int b) { return 128u * b; }
+    __device__ static constexpr uint32_t colO(int t) { return 128u * kSBufs + D * t; }
+    static_assert(128 * kSBufs + 2 * D <= 512, "TMEM budget");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr int kThreads = 320;  // warps 0-3 softmax 0, 4-7 softmax 1, 8 MMA, 9 TMA
     static constexpr int kWarpMma = 8;
     static constexpr int kWarpLoad = 9;
+};
+
+// The CTA's MMA jobs, in issue order: for each K/V tile j, tile 0 then tile 1 (each
+// only while that Q tile still needs keys). Q tile 1 never needs fewer K/V tiles
+// than Q tile 0 (n1 is 0, n0 or n0 + 1), so the order is dense:
+//   jobs 2j, 2j+1 for j < n0, then job 2*n0 for tile 1's extra diagonal tile.
+struct JobOrder {
+    int n0, n1;
+    __device__ int total() const { return n0 + n1; }
+    __device__ int job(int t, int j) const {
+        if (n1 == 0) return j;
+        return j < n0 ? 2 * j + t : 2 * n0 + (j - n0);
+    }
+    __device__ void tile_of(int g, int& t, int& j) const {
+        if (n1 == 0) { t = 0; j = g; }
+        else if (g < 2 * n0) { t = g & 1; j = g >> 1; }
+        else { t = 1; j = n0 + (g - 2 * n0); }
+    }
+    // The last job that reads K/V tile j (after it, the ring stage can be refilled).
+    __device__ int last_job(int j) const { return n1 == 0 ? j : job(1, j); }
+    // The first job that reads K/V tile j (the one that waits for its copy to land).
+    __device__ int first_job(int j) const { return (n1 == 0 || j < n0) ? job(0, j) : job(1, j); }
 };
 
 // Bounded wait state shared by all roles of one CTA.
@@ -127,7 +154,7 @@ static __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, c
 // Whole-warp bounded wait: every lane observes the phase; lane 0 decides when to
 // give up so that the outcome is warp-uniform.
 static __device__ __noinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                            uint32_t where, uint32_t iter) {
+                                            uint32_t where, uint32_t iter, bool honor_abort) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 0;; ++n) {
@@ -136,7 +163,7 @@ static __device__ __noinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity
         if ((n & 63u) == 63u) {
             uint32_t give_up = 0;
             if (lane == 0) {
-                if (*w.abort) give_up = 1;
+                if (honor_abort && *w.abort) give_up = 1;
                 else if (global_timer_ns() - t0 > kWaitTimeoutNs) give_up = 2;
             }
             give_up = __shfl_sync(0xffffffffu, give_up, 0);
@@ -149,10 +176,10 @@ static __device__ __noinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity
 }
 
 static __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                          uint32_t where, uint32_t iter) {
+                                          uint32_t where, uint32_t iter, bool honor_abort = true) {
     const bool done = mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
-    return wait_warp_slow(bar, parity, w, where, iter);
+    return wait_warp_slow(bar, parity, w, where, iter, honor_abort);
 }
 
 template <bool BF16>
@@ -164,6 +191,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&h);
     }
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Row maximum of 128 values held as 4 x 32 raw fp32 words (8 independent chains).
+__device__ __forceinline__ float row_max128(const uint32_t (&sr)[4][32]) {
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t* x = &sr[c >> 1][(c & 1) * 16];
+        float a = fmax3(__uint_as_float(x[0]), __uint_as_float(x[1]), __uint_as_float(x[2]));
+#pragma unroll
+        for (int k = 3; k < 15; k += 2) a = fmax3(a, __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+        acc[c] = fmaxf(a, __uint_as_float(x[15]));
+    }
+    return fmaxf(fmax3(acc[0], acc[1], acc[2]), fmax3(fmax3(acc[3], acc[4], acc[5]), acc[6], acc[7]));
 }
 
 template <int D, bool CAUSAL, bool BF16>
@@ -200,14 +247,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         n_kv[t] = valid ? n : 0;
     }
     const int n_max = max(n_kv[0], n_kv[1]);
+    const JobOrder jobs{n_kv[0], n_kv[1]};
 
     WaitCtx wc{p.err, misc + 1, blockIdx.x};
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
-            uint32_t count = 1;
-            if (i == C::kBarPFull || i == C::kBarPFull + 1) count = 128;
-            mbar_init(bar(i), count);
+            const bool p_full = i >= C::kBarPFull && i < C::kBarPFull + C::kSBufs;
+            mbar_init(bar(i), p_full ? 4u : 1u);  // P ready: one arrive per softmax warp
         }
         misc[1] = 0u;
         fence_mbar_init();
@@ -267,85 +314,67 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         __syncwarp();
     } else if (warp == C::kWarpMma) {
         // ================================ MMA issuer ==================================
-        if (lane == 0) {
+        // The whole warp walks the job list with warp-uniform values; elect.sync picks
+        // the lane that issues each tcgen05 instruction.
+        {
             constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, 128, 128, false);
             constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, 128, D, true);
+            // Descriptors of every operand buffer, built once; an MMA adds its byte
+            // offset (>> 4) to the start-address field.
+            const uint64_t dq0 = sdesc_sw128(sQ(0), 16, 1024), dq1 = sdesc_sw128(sQ(1), 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(sK(0), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sV(0), C::kBoxBytes, 1024);
+            constexpr uint64_t kStageStep = C::kTileBytes >> 4;
+
             bool ok = true;
             for (int t = 0; t < 2 && ok; ++t)
                 if (n_kv[t] > 0)
-                    ok = wait_one(bar(C::kBarQFull + t), 0, wc, kRoleMma * 1000 + C::kBarQFull + t, 0);
+                    ok = wait_warp(bar(C::kBarQFull + t), 0, wc, kRoleMma * 1000 + C::kBarQFull + t, 0);
             tc_fence_after_sync();
 
-            auto issue_s = [&](int t, int s) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(sQ(t) + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sK(s) + off, 16, 1024);
-                    mma_f16_ss(tmem + C::colS(t), a, b, idesc_s, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, int s, bool acc) {
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(sV(s) + kk * 2048, C::kBoxBytes, 1024);
-                    mma_f16_ts(tmem + C::colO(t), tmem + C::colS(t) + kk * 8, b, idesc_o,
-                               (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-
-            for (int j = 0; j < n_max && ok; ++j) {
+            const int G = jobs.total();
+            // S = Q_t K_j^T into S/P buffer g % kSBufs.
+            auto issue_s = [&](int g) -> bool {
+                int t, j;
+                jobs.tile_of(g, t, j);
                 const int s = j % C::kStages;
-                const uint32_t ph = (j / C::kStages) & 1;
-                if (!wait_one(bar(C::kBarKFull + s), ph, wc, kRoleMma * 1000 + C::kBarKFull + s, j)) {
+                if (!wait_warp(bar(C::kBarKFull + s), (j / C::kStages) & 1, wc,
+                               kRoleMma * 1000 + C::kBarKFull + s, g))
+                    return false;
+                tc_fence_after_sync();
+                const uint64_t a0 = t ? dq1 : dq0;
+                const uint64_t b0 = dk0 + s * kStageStep;
+                const uint32_t d = tmem + C::colS(g % C::kSBufs);
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    const uint64_t off = (c * C::kBoxBytes) >> 4;
+                    mma_qk64_warp(d, a0 + off, b0 + off, idesc_s, c > 0 ? 1u : 0u);
+                }
+                mma_commit_warp(bar(C::kBarSFull + g % C::kSBufs));
+                return true;
+            };
+            for (int g = 0; g < min(C::kSBufs, G) && ok; ++g) ok = issue_s(g);
+            for (int g = 0; g < G && ok; ++g) {
+                int t, j;
+                jobs.tile_of(g, t, j);
+                const int b = g % C::kSBufs;
+                const int s = j % C::kStages;
+                if (!wait_warp(bar(C::kBarPFull + b), (g / C::kSBufs) & 1, wc, kRoleMma * 1000 + C::kBarPFull + b, g) ||
+                    !wait_warp(bar(C::kBarVFull + s), (j / C::kStages) & 1, wc, kRoleMma * 1000 + C::kBarVFull + s, g)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                if (j < n_kv[0]) {
-                    issue_s(0, s);
-                    mma_commit(bar(C::kBarSFull + 0));
-                }
-                if (j >= 1 && j - 1 < n_kv[1]) {
-                    if (!wait_one(bar(C::kBarPFull + 1), (j - 1) & 1, wc, kRoleMma * 1000 + C::kBarPFull + 1, j)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    issue_pv(1, (j - 1) % C::kStages, j - 1 > 0);
-                    mma_commit(bar(C::kBarODone + 1));
-                }
-                if (j >= 1) mma_commit(bar(C::kBarKvEmpty + (j - 1) % C::kStages));
-                if (j < n_kv[1]) {
-                    issue_s(1, s);
-                    mma_commit(bar(C::kBarSFull + 1));
-                }
-                if (!wait_one(bar(C::kBarVFull + s), ph, wc, kRoleMma * 1000 + C::kBarVFull + s, j)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                if (j < n_kv[0]) {
-                    if (!wait_one(bar(C::kBarPFull + 0), j & 1, wc, kRoleMma * 1000 + C::kBarPFull, j)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    issue_pv(0, s, j > 0);
-                    mma_commit(bar(C::kBarODone + 0));
-                }
+                // O_t += P V_j, P (16-bit) read from the S/P buffer.
+                const uint64_t b0 = dv0 + s * kStageStep;
+                mma_pv128_warp(tmem + C::colO(t), tmem + C::colS(b), b0, idesc_o, j > 0 ? 1u : 0u);
+                mma_commit_warp(bar(C::kBarODone + t));
+                if (g == jobs.last_job(j)) mma_commit_warp(bar(C::kBarKvEmpty + s));
+                if (g + C::kSBufs < G) ok = issue_s(g + C::kSBufs);
             }
-            if (ok && n_max >= 1 && n_max - 1 < n_kv[1]) {
-                const int j = n_max;
-                if (wait_one(bar(C::kBarPFull + 1), (j - 1) & 1, wc, kRoleMma * 1000 + C::kBarPFull + 1, j)) {
-                    tc_fence_after_sync();
-                    issue_pv(1, (j - 1) % C::kStages, j - 1 > 0);
-                    mma_commit(bar(C::kBarODone + 1));
-                }
-            }
-            // Drain: all MMAs issued by this thread are complete before TMEM is freed.
-            mma_commit(bar(C::kBarDrain));
-            wait_one(bar(C::kBarDrain), 0, wc, kRoleMma * 1000 + C::kBarDrain, 0, false);
+            // Drain: all MMAs issued by this warp are complete before TMEM is freed.
+            mma_commit_warp(bar(C::kBarDrain));
+            wait_warp(bar(C::kBarDrain), 0, wc, kRoleMma * 1000 + C::kBarDrain, 0, false);
         }
         __syncwarp();
     } else {
@@ -355,15 +384,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const uint32_t r = wq * 32u + lane;       // row inside the Q tile = TMEM lane
         const int q_row = row0[t] + static_cast<int>(r);
         const uint32_t role = t == 0 ? kRoleSoftmax0 : kRoleSoftmax1;
-        const uint32_t tS = tmem_addr(tmem, wq * 32u, C::colS(t));
-        const uint32_t tO = tmem_addr(tmem, wq * 32u, C::colO(t));
+        const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
+        const uint32_t tO = lane_base + C::colO(t);
         const float qk = p.qk_scale;
+        const float2 qk2 = make_float2(qk, qk);
 
         bool ok = n_kv[t] > 0;
         float m = -INFINITY;  // running max, log2 units of the scaled scores (possibly stale)
         float l = 0.f;        // running sum of P (fp32), relative to m
         for (int j = 0; j < n_kv[t] && ok; ++j) {
-            if (!wait_warp(bar(C::kBarSFull + t), j & 1, wc, role * 1000 + C::kBarSFull + t, j)) {
+            const int g = jobs.job(t, j);
+            const int b = g % C::kSBufs;
+            const uint32_t tS = lane_base + C::colS(b);
+            if (!wait_warp(bar(C::kBarSFull + b), (g / C::kSBufs) & 1, wc, role * 1000 + C::kBarSFull + b, j)) {
                 ok = false;
                 break;
             }
@@ -378,56 +411,50 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const int k0 = j * C::BN;
             const bool need_mask = (k0 + C::BN > N) || (CAUSAL && k0 + C::BN - 1 > row0[t]);
             if (need_mask) {
+                const int lim = CAUSAL ? min(N, q_row + 1) : N;  // keys [k0, lim) are visible
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int kp = k0 + c * 32 + e;
-                        const bool keep = kp < N && (!CAUSAL || kp <= q_row);
-                        if (!keep) sr[c][e] = __float_as_uint(-INFINITY);
-                    }
+                    for (int e = 0; e < 32; ++e)
+                        if (k0 + c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
             }
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i >> 1][(i & 1) * 16]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int i = (c * 2 + (e >> 4)) & 7;
-                    mx[i] = fmaxf(mx[i], __uint_as_float(sr[c][e]));
-                }
-            const float row_max =
-                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float row_max = row_max128(sr);
             float m_new = fmaxf(m, row_max * qk);
             if (m_new - m <= kRescaleTau) m_new = m;  // keep the stale max (false when m = -inf)
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             // rescale factor of the old state; exactly 1 when the maximum is kept
             const float alpha = (m == m_use) ? 1.f : ex2_ftz(m - m_use);
+            const float2 neg_m2 = make_float2(-m_use, -m_use);
 
             uint32_t pk[2][32];
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                const float x0 = __uint_as_float(sr[(2 * i) >> 5][(2 * i) & 31]);
-                const float x1 = __uint_as_float(sr[(2 * i + 1) >> 5][(2 * i + 1) & 31]);
-                const float p0 = ex2_ftz(fmaf(x0, qk, -m_use));
-                const float p1 = ex2_ftz(fmaf(x1, qk, -m_use));
-                sum[i & 3] += p0 + p1;
-                pk[i >> 5][i & 31] = pack2<BF16>(p0, p1);
+                const float2 x = make_float2(__uint_as_float(sr[(2 * i) >> 5][(2 * i) & 31]),
+                                             __uint_as_float(sr[(2 * i + 1) >> 5][(2 * i + 1) & 31]));
+                const float2 y = __ffma2_rn(x, qk2, neg_m2);
+                const float2 pr = make_float2(ex2_ftz(y.x), ex2_ftz(y.y));
+                sum2[i & 1] = __fadd2_rn(sum2[i & 1], pr);
+                pk[i >> 5][i & 31] = pack2<BF16>(pr.x, pr.y);
             }
-            l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+            const float2 s2 = __fadd2_rn(sum2[0], sum2[1]);
+            l = l * alpha + (s2.x + s2.y);
             tmem_st32(tS, pk[0]);
             tmem_st32(tS + 32, pk[1]);
             tmem_st_wait();
 
+            // Wait for O += P(j-1) V to finish at every job, not only when rescaling:
+            // with rotating S/P buffers this warpgroup can run ahead of the MMAs of
+            // its own tile, and o_done is only unambiguous while its waiter stays at
+            // most one phase behind.
+            if (j > 0 && !wait_warp(bar(C::kBarODone + t), (j - 1) & 1, wc, role * 1000 + C::kBarODone + t, j)) {
+                ok = false;
+                break;
+            }
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O still holds the sum up to tile j-1 scaled by the old max.
-                if (!wait_warp(bar(C::kBarODone + t), (j - 1) & 1, wc, role * 1000 + C::kBarODone + t, j)) {
-                    ok = false;
-                    break;
-                }
+                // O holds the sum up to tile j-1 scaled by the old max.
                 tc_fence_after_sync();
+                const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -435,14 +462,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                     tmem_ld_wait();
                     reg_fence(o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                        o[e] = __float_as_uint(v.x);
+                        o[e + 1] = __float_as_uint(v.y);
+                    }
                     tmem_st32(tO + c * 32, o);
                 }
                 tmem_st_wait();
             }
             m = m_new;
+            // Every lane's TMEM stores are complete (wait::st) and fenced; the warp
+            // barrier orders them before lane 0's release-arrive.
             tc_fence_before_sync();
-            mbar_arrive(bar(C::kBarPFull + t));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarPFull + b));
         }
 
         // ---- epilogue: O / l -> dtype -> swizzled SMEM (reusing this Q tile) -> TMA store

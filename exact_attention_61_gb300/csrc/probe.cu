@@ -52,16 +52,14 @@ __global__ void __launch_bounds__(128, 1)
         }
     }
     bool ok = wait_warp(bars, 0, wc, 1, 0);
-    if (ok && threadIdx.x == 0) {
+    if (ok && warp == 0) {
         tc_fence_after_sync();
         constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, 128, 128, false);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_f16_ss(tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idesc_s,
-                       kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bars + 8);
+        for (int c = 0; c < D / 64; ++c)
+            mma_qk64_warp(tmem, sdesc_sw128(sQ + c * kBox, 16, 1024), sdesc_sw128(sK + c * kBox, 16, 1024),
+                          idesc_s, c > 0 ? 1u : 0u);
+        mma_commit_warp(bars + 8);
     }
     if (ok) ok = wait_warp(bars + 8, 0, wc, 2, 0);
     const uint32_t tS = tmem_addr(tmem, warp * 32u, 0);
@@ -86,14 +84,11 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_before_sync();
     __syncthreads();
     ok = ok && misc[1] == 0u;
-    if (ok && threadIdx.x == 0) {
+    if (ok && warp == 0) {
         tc_fence_after_sync();
         constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, 128, D, true);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ts(tmem + 128, tmem + kk * 8, sdesc_sw128(sV + kk * 2048, kBox, 1024), idesc_o,
-                       kk > 0 ? 1u : 0u);
-        mma_commit(bars + 16);
+        mma_pv128_warp(tmem + 128, tmem, sdesc_sw128(sV, kBox, 1024), idesc_o, 0u);
+        mma_commit_warp(bars + 16);
     }
     if (ok) ok = wait_warp(bars + 16, 0, wc, 3, 0);
     if (ok) {
@@ -108,9 +103,9 @@ __global__ void __launch_bounds__(128, 1)
         }
     }
     // Drain the tensor core before freeing TMEM (covers an aborted run too).
-    if (threadIdx.x == 0) {
-        mma_commit(bars + 16);
-        wait_one(bars + 16, ok ? 1 : 0, wc, 4, 0, false);
+    if (warp == 0) {
+        mma_commit_warp(bars + 16);
+        wait_warp(bars + 16, ok ? 1 : 0, wc, 4, 0, false);
     }
     tc_fence_before_sync();
     __syncthreads();

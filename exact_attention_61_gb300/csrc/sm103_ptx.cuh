@@ -66,6 +66,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test (never suspends the thread): true if the phase has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ----------------------------------------------------------------------------------------
 // TMA (bulk tensor copies)
 // ----------------------------------------------------------------------------------------
@@ -181,6 +194,94 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-wide forms: every lane of the warp executes the call with the same
+// (warp-uniform) operands, and one lane chosen by elect.sync issues the
+// instruction. Keeping the operands warp-uniform lets them live in uniform
+// registers, which the tcgen05 instructions read directly.
+__device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+// One group of MMAs issued back to back from a single asm block, so that no
+// compiler scheduling barrier sits between them. Warp-wide; elect.sync picks the
+// issuing lane. Descriptor steps are in 16-byte units (the start-address field).
+//
+// P V over 128 keys: 8 MMAs of K = 16; A (P, 16-bit) advances 8 TMEM columns and
+// B (V, MN-major) advances 16 rows = 2048 bytes per MMA. `accumulate` applies to
+// the first MMA; the rest always accumulate.
+__device__ __forceinline__ void mma_pv128_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, one;\n\t.reg .b32 ta;\n\t.reg .b64 bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 one, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.u64 bd, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.u64 bd, %2, 256;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.u64 bd, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 32;\n\tadd.u64 bd, %2, 512;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 40;\n\tadd.u64 bd, %2, 640;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 48;\n\tadd.u64 bd, %2, 768;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 56;\n\tadd.u64 bd, %2, 896;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// S = Q K^T over a 64-wide slice of the head dimension: 4 MMAs of K = 16, both
+// operands K-major in one 128-byte-swizzled box, advancing 32 bytes (2 units) each.
+// `accumulate` applies to the first MMA.
+__device__ __forceinline__ void mma_qk64_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, one;\n\t.reg .b64 ad, bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 one, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.u64 ad, %1, 2;\n\tadd.u64 bd, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 4;\n\tadd.u64 bd, %2, 4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 6;\n\tadd.u64 bd, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
