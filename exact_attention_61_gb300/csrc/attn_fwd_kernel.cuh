@@ -67,7 +67,8 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-    // barriers: q_full[2] k_full[St] v_full[St] kv_empty[St] s_full[Sb] p_full[Sb] o_done[2] drain
+    // barriers: q_full[2] k_full[St] v_full[St] kv_empty[St] s_full[Sb] p_full[Sb] o_done[2]
+    //           o_final[2] drain
     static constexpr int kBarQFull = 0;
     static constexpr int kBarKFull = 2;
     static constexpr int kBarVFull = kBarKFull + kStages;
@@ -75,7 +76,8 @@ struct FwdCfg {
     static constexpr int kBarSFull = kBarKvEmpty + kStages;
     static constexpr int kBarPFull = kBarSFull + kSBufs;
     static constexpr int kBarODone = kBarPFull + kSBufs;
-    static constexpr int kBarDrain = kBarODone + 2;
+    static constexpr int kBarOFinal = kBarODone + 2;
+    static constexpr int kBarDrain = kBarOFinal + 2;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
@@ -369,6 +371,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 const uint64_t b0 = dv0 + s * kStageStep;
                 mma_pv128_warp(tmem + C::colO(t), tmem + C::colS(b), b0, idesc_o, j > 0 ? 1u : 0u);
                 mma_commit_warp(bar(C::kBarODone + t));
+                if (j == n_kv[t] - 1) mma_commit_warp(bar(C::kBarOFinal + t));
                 if (g == jobs.last_job(j)) mma_commit_warp(bar(C::kBarKvEmpty + s));
                 if (g + C::kSBufs < G) ok = issue_s(g + C::kSBufs);
             }
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const float2 qk2 = make_float2(qk, qk);
 
         bool ok = n_kv[t] > 0;
+        const bool single_tile = n_kv[1] == 0;
         float m = -INFINITY;  // running max, log2 units of the scaled scores (possibly stale)
         float l = 0.f;        // running sum of P (fp32), relative to m
         for (int j = 0; j < n_kv[t] && ok; ++j) {
@@ -443,16 +447,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             tmem_st32(tS + 32, pk[1]);
             tmem_st_wait();
 
-            // Wait for O += P(j-1) V to finish at every job, not only when rescaling:
-            // with rotating S/P buffers this warpgroup can run ahead of the MMAs of
-            // its own tile, and o_done is only unambiguous while its waiter stays at
-            // most one phase behind.
-            if (j > 0 && !wait_warp(bar(C::kBarODone + t), (j - 1) & 1, wc, role * 1000 + C::kBarODone + t, j)) {
+            // Before O is rescaled, the last O += P V into it must be complete. With
+            // both Q tiles active the jobs interleave, so S of this job was issued
+            // after O += P(j-2) V and waiting for that S leaves o_done with j-1 or j
+            // completed phases: one parity wait is unambiguous. With one Q tile the
+            // jobs are consecutive and this warpgroup may run two jobs ahead of its
+            // O += P V; it then waits at every job so that it never falls behind.
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+            if ((rescale || (single_tile && j > 0)) &&
+                !wait_warp(bar(C::kBarODone + t), (j - 1) & 1, wc, role * 1000 + C::kBarODone + t, j)) {
                 ok = false;
                 break;
             }
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O holds the sum up to tile j-1 scaled by the old max.
+            if (rescale) {
                 tc_fence_after_sync();
                 const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
@@ -481,7 +488,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
         // ---- epilogue: O / l -> dtype -> swizzled SMEM (reusing this Q tile) -> TMA store
         if (ok) {
-            ok = wait_warp(bar(C::kBarODone + t), (n_kv[t] - 1) & 1, wc, role * 1000 + 70, n_kv[t]);
+            // o_final completes once, after the last O += P V of this tile.
+            ok = wait_warp(bar(C::kBarOFinal + t), 0, wc, role * 1000 + C::kBarOFinal + t, n_kv[t]);
         }
         if (ok) {
             tc_fence_after_sync();

@@ -9,7 +9,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "attn_internal.h"
 
 namespace attn_sm103 {

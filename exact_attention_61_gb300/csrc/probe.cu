@@ -3,8 +3,8 @@
 // descriptors and TMEM layouts (see include/attn_probe.h).
 #include <cuda_runtime.h>
 
-#include "../../include/attn.h"
-#include "../../include/attn_probe.h"
+#include "attn.h"
+#include "attn_probe.h"
 #include "attn_fwd_kernel.cuh"
 #include "attn_internal.h"
 

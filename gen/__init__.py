@@ -1,3 +1,3 @@
 """Seeded synthetic inputs shared by the oracle tests, the CUDA-path tests and the bench."""
-from .inputs import (WORKLOADS, Workload, make_qkv, sweep_points, sweep_seed,  # noqa: F401
-                     to_dtype, workload)
+from .inputs import (WORKLOADS, Workload, make_qkv, make_qkv_rising, sweep_points,  # noqa: F401
+                     sweep_seed, to_dtype, workload)

@@ -98,3 +98,22 @@ def make_qkv(B: int, H: int, N: int, d: int, dtype: str, seed: int,
             x.mul_(input_scale)
         out.append(x.to(to_dtype(dtype)).contiguous())
     return tuple(out)
+
+
+def make_qkv_rising(B: int, H: int, N: int, d: int, dtype: str, seed: int, step: float = 1.0):
+    """Q, K, V whose scores rise along the keys, so that every 128-key tile raises the
+    running row maximum by more than the kernel's lazy-rescale threshold (exercises the
+    online rescaling on every tile).
+
+    Q ~ N(0,1) + 1 and K[j] ~ N(0,1) + step * (j / 128) * 8 / sqrt(d) on every
+    component; V ~ N(0,1). Drawn in fp32 from one seeded generator (Q, K, V in that
+    order), then rounded to dtype.
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    q = torch.randn((B, H, N, d), generator=g, dtype=torch.float32) + 1.0
+    k = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+    ramp = torch.arange(N, dtype=torch.float32).div_(128.0).mul_(step * 8.0 / d ** 0.5)
+    k.add_(ramp.view(1, 1, N, 1))
+    dt = to_dtype(dtype)
+    return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()

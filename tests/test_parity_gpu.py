@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from gen import WORKLOADS, make_qkv, sweep_points, workload
+from gen import make_qkv, make_qkv_rising, sweep_points, workload
 
 TOL_O = {"fp16": 4e-3, "bf16": 3.2e-2}
 TOL_LSE = 1e-3
@@ -161,3 +161,21 @@ def test_rejects_bad_device_arguments(cuda_lib):
     q, k, v = (t.cuda() for t in make_qkv(1, 1, 64, 64, "bf16", seed=1))
     with pytest.raises(AttnError):
         cuda_lib.fwd(q, k, v, scale=-1.0)
+
+
+# ---- online rescaling on every tile ------------------------------------------------------------
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N", [200, 384, 513, 1000, 2048])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rising_scores_rescale_every_tile(cuda_lib, N, d, dtype, causal):
+    """Scores rise along the keys, so each key tile raises the row maximum by more than
+    the lazy-rescale threshold: O is rescaled in TMEM on every tile. N=384 and N=513
+    leave the last CTA with a single Q tile."""
+    q, k, v = make_qkv_rising(1, 2, N, d, dtype, seed=7000 + N + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(cuda_lib, q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    _report(f"rising N{N}d{d}{dtype}{'c' if causal else ''}", o, lse, o_ref, lse_ref, dtype)
