@@ -132,7 +132,7 @@ static __device__ __noinline__ void record_timeout(const WaitCtx& w, uint32_t wh
 
 // Single-thread bounded wait. With honor_abort, gives up as soon as another role of
 // the CTA has given up; without it (draining), waits for the phase up to the timeout.
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                        uint32_t where, uint32_t iter, bool honor_abort) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 0;; ++n) {
@@ -155,7 +155,7 @@ static __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, c
 
 // Whole-warp bounded wait: every lane observes the phase; lane 0 decides when to
 // give up so that the outcome is warp-uniform.
-static __device__ __noinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+static __device__ __forceinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                             uint32_t where, uint32_t iter, bool honor_abort) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t t0 = global_timer_ns();
@@ -240,16 +240,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const int ct = p.n_ctiles - 1 - static_cast<int>(blockIdx.x / static_cast<uint32_t>(p.BH));
     const int N = p.N;
     const int n_kv_all = (N + C::BN - 1) / C::BN;
-    int row0[2], n_kv[2];
-    for (int t = 0; t < 2; ++t) {
-        row0[t] = ct * C::kRowsPerCta + t * C::BM;
-        const bool valid = row0[t] < N;
-        int n = n_kv_all;
-        if (CAUSAL) n = min(n_kv_all, row0[t] / C::BN + 1);
-        n_kv[t] = valid ? n : 0;
-    }
-    const int n_max = max(n_kv[0], n_kv[1]);
-    const JobOrder jobs{n_kv[0], n_kv[1]};
+    // First query row and number of key tiles of each Q tile (kept in scalars: an
+    // array indexed by the tile would live in local memory).
+    const int row0_0 = ct * C::kRowsPerCta, row0_1 = row0_0 + C::BM;
+    const int nkv_0 = CAUSAL ? min(n_kv_all, row0_0 / C::BN + 1) : n_kv_all;
+    const int nkv_1 = row0_1 < N ? (CAUSAL ? min(n_kv_all, row0_1 / C::BN + 1) : n_kv_all) : 0;
+    auto row0 = [&](int t) { return t ? row0_1 : row0_0; };
+    auto n_kv = [&](int t) { return t ? nkv_1 : nkv_0; };
+    const int n_max = max(nkv_0, nkv_1);
+    const JobOrder jobs{nkv_0, nkv_1};
 
     WaitCtx wc{p.err, misc + 1, blockIdx.x};
 
@@ -279,11 +278,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
             for (int t = 0; t < 2; ++t) {
-                if (n_kv[t] == 0) continue;
+                if (n_kv(t) == 0) continue;
                 mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d_hint(sQ(t) + c * C::kBoxBytes, &tmQ, bar(C::kBarQFull + t), c * 64,
-                                     row0[t], bh, pol_q);
+                                     row0(t), bh, pol_q);
             }
             int issued = 0;
             for (int j = 0; j < n_max; ++j) {
@@ -305,7 +304,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             // Drain: every copy issued into this CTA's shared memory has landed before
             // the CTA can exit (on the normal path these phases completed long ago).
             for (int t = 0; t < 2; ++t)
-                if (n_kv[t] > 0) wait_one(bar(C::kBarQFull + t), 0, wc, kRoleLoad * 1000 + 90 + t, 0, false);
+                if (n_kv(t) > 0) wait_one(bar(C::kBarQFull + t), 0, wc, kRoleLoad * 1000 + 90 + t, 0, false);
             for (int jj = max(0, issued - C::kStages); jj < issued; ++jj) {
                 const int s = jj % C::kStages;
                 const uint32_t ph = (jj / C::kStages) & 1;
@@ -330,7 +329,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
             bool ok = true;
             for (int t = 0; t < 2 && ok; ++t)
-                if (n_kv[t] > 0)
+                if (n_kv(t) > 0)
                     ok = wait_warp(bar(C::kBarQFull + t), 0, wc, kRoleMma * 1000 + C::kBarQFull + t, 0);
             tc_fence_after_sync();
 
@@ -371,7 +370,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 const uint64_t b0 = dv0 + s * kStageStep;
                 mma_pv128_warp(tmem + C::colO(t), tmem + C::colS(b), b0, idesc_o, j > 0 ? 1u : 0u);
                 mma_commit_warp(bar(C::kBarODone + t));
-                if (j == n_kv[t] - 1) mma_commit_warp(bar(C::kBarOFinal + t));
+                if (j == n_kv(t) - 1) mma_commit_warp(bar(C::kBarOFinal + t));
                 if (g == jobs.last_job(j)) mma_commit_warp(bar(C::kBarKvEmpty + s));
                 if (g + C::kSBufs < G) ok = issue_s(g + C::kSBufs);
             }
@@ -385,18 +384,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int t = static_cast<int>(warp >> 2);
         const uint32_t wq = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = wq * 32u + lane;       // row inside the Q tile = TMEM lane
-        const int q_row = row0[t] + static_cast<int>(r);
+        const int q_row = row0(t) + static_cast<int>(r);
         const uint32_t role = t == 0 ? kRoleSoftmax0 : kRoleSoftmax1;
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
         const uint32_t tO = lane_base + C::colO(t);
         const float qk = p.qk_scale;
         const float2 qk2 = make_float2(qk, qk);
 
-        bool ok = n_kv[t] > 0;
-        const bool single_tile = n_kv[1] == 0;
+        bool ok = n_kv(t) > 0;
+        const bool single_tile = nkv_1 == 0;
         float m = -INFINITY;  // running max, log2 units of the scaled scores (possibly stale)
         float l = 0.f;        // running sum of P (fp32), relative to m
-        for (int j = 0; j < n_kv[t] && ok; ++j) {
+        for (int j = 0; j < n_kv(t) && ok; ++j) {
             const int g = jobs.job(t, j);
             const int b = g % C::kSBufs;
             const uint32_t tS = lane_base + C::colS(b);
@@ -413,7 +412,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
 
             const int k0 = j * C::BN;
-            const bool need_mask = (k0 + C::BN > N) || (CAUSAL && k0 + C::BN - 1 > row0[t]);
+            const bool need_mask = (k0 + C::BN > N) || (CAUSAL && k0 + C::BN - 1 > row0(t));
             if (need_mask) {
                 const int lim = CAUSAL ? min(N, q_row + 1) : N;  // keys [k0, lim) are visible
 #pragma unroll
@@ -489,7 +488,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         // ---- epilogue: O / l -> dtype -> swizzled SMEM (reusing this Q tile) -> TMA store
         if (ok) {
             // o_final completes once, after the last O += P V of this tile.
-            ok = wait_warp(bar(C::kBarOFinal + t), 0, wc, role * 1000 + C::kBarOFinal + t, n_kv[t]);
+            ok = wait_warp(bar(C::kBarOFinal + t), 0, wc, role * 1000 + C::kBarOFinal + t, n_kv(t));
         }
         if (ok) {
             tc_fence_after_sync();
@@ -519,11 +518,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             }
         }
         fence_proxy_async_smem();
-        if (n_kv[t] > 0) named_bar_sync(1 + t, 128);
-        if (n_kv[t] > 0 && wq == 0 && lane == 0 && *wc.abort == 0u) {
+        if (n_kv(t) > 0) named_bar_sync(1 + t, 128);
+        if (n_kv(t) > 0 && wq == 0 && lane == 0 && *wc.abort == 0u) {
             tma_prefetch_desc(&tmO);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_store_3d(&tmO, sQ(t) + c * C::kBoxBytes, c * 64, row0[t], bh);
+                tma_store_3d(&tmO, sQ(t) + c * C::kBoxBytes, c * 64, row0(t), bh);
             tma_store_commit();
             tma_store_wait_all();
         }
