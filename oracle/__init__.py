@@ -73,6 +73,10 @@ def _load():
                                              ctypes.c_int64, ctypes.c_int, ctypes.c_double,
                                              _I64P, ctypes.c_int64, _DP, _DP]
             lib.oracle_attn_rows.restype = ctypes.c_int
+            lib.oracle_attn_fwd_qk.argtypes = [_DP, _DP, _DP, _DP, _DP, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_int, ctypes.c_double]
+            lib.oracle_attn_fwd_qk.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -114,6 +118,49 @@ def attn_fwd(q, k, v, causal: bool, scale: float | None = None):
                                  B, H, N, d, int(bool(causal)), scale)
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd failed with code {rc}")
+    return o, lse
+
+
+def attn_fwd_qk(q, k, v, causal: bool, scale: float | None = None):
+    """Nq query rows [B,H,Nq,d] against Nk keys [B,H,Nk,d] (C, fp64).
+
+    Under the causal mask the query rows are the last Nq positions of the Nk-long
+    sequence: row i sees keys j <= i + Nk - Nq. A row with no visible key gets
+    O = 0 and LSE = -inf. Returns (O [B,H,Nq,d], LSE [B,H,Nq]).
+    """
+    q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
+    B, H, Nq, d = q64.shape
+    Bk, Hk, Nk, dk = k64.shape
+    if (Bk, Hk, dk) != (B, H, d) or v64.shape != k64.shape:
+        raise ValueError("q [B,H,Nq,d], k and v [B,H,Nk,d] must agree on B, H, d")
+    scale = default_scale(d) if scale is None else float(scale)
+    o = np.empty_like(q64)
+    lse = np.empty((B, H, Nq), dtype=np.float64)
+    rc = _load().oracle_attn_fwd_qk(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(o), _ptr(lse),
+                                    B * H, Nq, Nk, d, int(bool(causal)), scale)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_qk failed with code {rc}")
+    return o, lse
+
+
+def attn_fwd_qk_materialised(q, k, v, causal: bool, scale: float | None = None):
+    """numpy fp64 twin of :func:`attn_fwd_qk` with the whole Nq x Nk score matrix."""
+    q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
+    B, H, Nq, d = q64.shape
+    Nk = k64.shape[2]
+    scale = default_scale(d) if scale is None else float(scale)
+    s = scale * np.einsum("bhid,bhjd->bhij", q64, k64)
+    keep = np.ones((Nq, Nk), dtype=bool)
+    if causal:
+        keep = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    s = np.where(keep, s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    e = np.exp(s - m_safe)
+    l = e.sum(axis=-1, keepdims=True)
+    o = np.einsum("bhij,bhjd->bhid", e, v64) / np.where(empty, 1.0, l)
+    lse = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, l)))[..., 0]
     return o, lse
 
 

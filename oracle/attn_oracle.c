@@ -29,6 +29,15 @@
  * Inputs are fp64 arrays, row-major [B*H][N][d]; callers upcast the 16-bit
  * tensors exactly before the call. Every row has at least one visible key
  * (key 0, and key i itself under the causal mask), so m and l are finite.
+ *
+ * oracle_attn_fwd_qk generalises to Nq query rows against Nk keys (the query
+ * rows of "Programming an attention kernel in Triton", Kernel 4, may be fewer
+ * or more than the keys). Under the causal mask the query rows are taken to be
+ * the LAST Nq positions of the Nk-long sequence (a KV-cache decode step, the
+ * extension named at the end of "Getting the kernel correct, then benchmarking
+ * it honestly"): row i sees keys j <= i + Nk - Nq. With Nq = Nk this is the
+ * top-left mask above. A row that sees no key (only when causal and Nq > Nk)
+ * gets O = 0 and LSE = -inf.
  */
 #include <math.h>
 #include <stdint.h>
@@ -128,6 +137,71 @@ int oracle_attn_rows(const double* q, const double* k, const double* v,
                 const int64_t bh = rows[r] / N, i = rows[r] % N;
                 oracle_row(q + rows[r] * d, k + bh * N * d, v + bh * N * d, N, d, i, causal,
                            scale, s, o + r * d, lse + r);
+            }
+            free(s);
+        }
+    }
+    return failed ? -2 : 0;
+}
+
+/* Query row i of one head against keys [0, n_vis) (n_vis may be 0). */
+static void oracle_row_n(const double* qi, const double* K, const double* V, int64_t d,
+                         int64_t n_vis, double scale, double* s, double* oi, double* lse_i)
+{
+    if (n_vis <= 0) {
+        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+        *lse_i = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        const double* kj = K + j * d;
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t) dot += qi[t] * kj[t];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        s[j] = exp(s[j] - m);
+        l += s[j];
+    }
+    for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        const double e = s[j];
+        const double* vj = V + j * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] += e * vj[t];
+    }
+    for (int64_t t = 0; t < d; ++t) oi[t] /= l;
+    *lse_i = m + log(l);
+}
+
+/* Nq query rows against Nk keys: q, o [BH][Nq][d]; k, v [BH][Nk][d]; lse [BH][Nq].
+ * Causal: row i sees keys j <= i + Nk - Nq. */
+int oracle_attn_fwd_qk(const double* q, const double* k, const double* v, double* o,
+                       double* lse, int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                       double scale)
+{
+    if (!q || !k || !v || !o || !lse || BH < 1 || Nq < 1 || Nk < 1 || d < 1) return -1;
+    if (!(scale > 0.0) || !isfinite(scale)) return -1;
+    int failed = 0;
+#pragma omp parallel reduction(| : failed)
+    {
+        double* s = (double*)malloc((size_t)Nk * sizeof(double));
+        if (!s) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4) collapse(2)
+            for (int64_t bh = 0; bh < BH; ++bh) {
+                for (int64_t i = 0; i < Nq; ++i) {
+                    int64_t n_vis = Nk;
+                    if (causal) {
+                        const int64_t last = i + Nk - Nq;  /* last visible key */
+                        n_vis = last < 0 ? 0 : (last + 1 < Nk ? last + 1 : Nk);
+                    }
+                    oracle_row_n(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * d, d, n_vis,
+                                 scale, s, o + (bh * Nq + i) * d, lse + bh * Nq + i);
+                }
             }
             free(s);
         }

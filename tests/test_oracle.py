@@ -247,3 +247,75 @@ def test_pins_catch_planted_mistakes(mistake):
     assert _pins_pass(lambda *a: oracle.attn_fwd_materialised(*a))
     assert _pins_pass(lambda *a: oracle.attn_fwd(*a))
     assert not _pins_pass(lambda q, k, v, c, s: _mutant_forward(q, k, v, c, s, mistake))
+
+
+# --- Nq query rows against Nk keys (decode and cross lengths) -------------------------------
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 10), (5, 15), (1, 64), (7, 300), (64, 64), (40, 25)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_qk_matches_materialised(Nq, Nk, causal):
+    """Includes the shapes of "Programming an attention kernel in Triton", Kernel 4:
+    Q (5, 32) against K/V (15, 32), and a single query (1, 64) against (10, 64)."""
+    g = np.random.default_rng(Nq * 1000 + Nk)
+    d = 32
+    q = g.standard_normal((2, 2, Nq, d))
+    k = g.standard_normal((2, 2, Nk, d))
+    v = g.standard_normal((2, 2, Nk, d))
+    o, lse = oracle.attn_fwd_qk(q, k, v, causal, 0.3)
+    o2, lse2 = oracle.attn_fwd_qk_materialised(q, k, v, causal, 0.3)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=TIGHT)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(lse2))
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(lse[fin], lse2[fin], rtol=0, atol=TIGHT)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(3, 50), (1, 128), (20, 20)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_qk_matches_torch_sdpa_explicit_mask(Nq, Nk, causal):
+    """Independent library check with an explicit boolean mask (torch's own is_causal
+    aligns top-left for Nq != Nk, so the bottom-right mask is spelled out)."""
+    q, _, _ = make_qkv(1, 2, Nq, 64, "bf16", seed=Nq)
+    _, k, v = make_qkv(1, 2, Nk, 64, "bf16", seed=Nk + 1)
+    o, lse = oracle.attn_fwd_qk(q, k, v, causal, 0.125)
+    q64, k64, v64 = (t.to(torch.float64) for t in (q, k, v))
+    mask = torch.ones(Nq, Nk, dtype=torch.bool)
+    if causal:
+        mask = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None] + (Nk - Nq)
+    ref = torch.nn.functional.scaled_dot_product_attention(q64, k64, v64, attn_mask=mask, scale=0.125)
+    s = (0.125 * (q64 @ k64.transpose(-1, -2))).masked_fill(~mask, float("-inf"))
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_qk_reduces_to_square_and_last_row_sees_all():
+    q, k, v = _rand64(1, 2, 33, 8, seed=41)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal)
+        o2, lse2 = oracle.attn_fwd_qk(q, k, v, causal)
+        np.testing.assert_array_equal(o, o2)
+        np.testing.assert_array_equal(lse, lse2)
+    # decode: the last query row under the bottom-right causal mask sees every key
+    g = np.random.default_rng(3)
+    qd = g.standard_normal((1, 1, 4, 8))
+    oc, lc = oracle.attn_fwd_qk(qd, k[:, :1], v[:, :1], True)
+    on, ln = oracle.attn_fwd_qk(qd, k[:, :1], v[:, :1], False)
+    np.testing.assert_array_equal(oc[:, :, -1], on[:, :, -1])
+    np.testing.assert_array_equal(lc[:, :, -1], ln[:, :, -1])
+    # and row i sees exactly i + Nk - Nq + 1 keys: zero queries give the mean of those
+    z = np.zeros((1, 1, 4, 8))
+    oz, lz = oracle.attn_fwd_qk(z, k[:, :1], v[:, :1], True)
+    for i in range(4):
+        n_vis = i + 33 - 4 + 1
+        np.testing.assert_allclose(oz[0, 0, i], v[0, 0, :n_vis].mean(axis=0), atol=1e-14)
+        assert abs(lz[0, 0, i] - math.log(n_vis)) < 1e-14
+
+
+def test_qk_rows_without_keys():
+    """More query rows than keys under the causal mask: the first Nq - Nk rows see no
+    key and get O = 0, LSE = -inf; the others see keys up to their diagonal."""
+    q, _, _ = _rand64(1, 1, 6, 4, seed=8)
+    _, k, v = _rand64(1, 1, 2, 4, seed=9)
+    o, lse = oracle.attn_fwd_qk(q, k, v, True)
+    assert np.all(o[0, 0, :4] == 0) and np.all(np.isneginf(lse[0, 0, :4]))
+    np.testing.assert_allclose(o[0, 0, 4], v[0, 0, 0], atol=1e-15)
+    assert np.isfinite(lse[0, 0, 5])
