@@ -121,12 +121,18 @@ def attn_fwd(q, k, v, causal: bool, scale: float | None = None):
     return o, lse
 
 
-def attn_fwd_qk(q, k, v, causal: bool, scale: float | None = None):
+_ALIGN = {"bottom_right": 1, "top_left": 2}
+
+
+def attn_fwd_qk(q, k, v, causal: bool, scale: float | None = None, align: str = "bottom_right"):
     """Nq query rows [B,H,Nq,d] against Nk keys [B,H,Nk,d] (C, fp64).
 
-    Under the causal mask the query rows are the last Nq positions of the Nk-long
-    sequence: row i sees keys j <= i + Nk - Nq. A row with no visible key gets
-    O = 0 and LSE = -inf. Returns (O [B,H,Nq,d], LSE [B,H,Nq]).
+    Under the causal mask with ``align="bottom_right"`` the query rows are the last
+    Nq positions of the Nk-long sequence: row i sees keys j <= i + Nk - Nq (a
+    KV-cache decode step). With ``align="top_left"`` row i sees keys j <= i, the
+    k_pos <= q_pos test of the profile-driven FlashAttention-2 page ("Round 4 /
+    Causal tile-skipping") applied to its separate N_QUERIES and N_KEYS. A row with
+    no visible key gets O = 0 and LSE = -inf. Returns (O [B,H,Nq,d], LSE [B,H,Nq]).
     """
     q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
     B, H, Nq, d = q64.shape
@@ -137,14 +143,16 @@ def attn_fwd_qk(q, k, v, causal: bool, scale: float | None = None):
     o = np.empty_like(q64)
     lse = np.empty((B, H, Nq), dtype=np.float64)
     rc = _load().oracle_attn_fwd_qk(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(o), _ptr(lse),
-                                    B * H, Nq, Nk, d, int(bool(causal)), scale)
+                                    B * H, Nq, Nk, d, _ALIGN[align] if causal else 0, scale)
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd_qk failed with code {rc}")
     return o, lse
 
 
-def attn_fwd_qk_materialised(q, k, v, causal: bool, scale: float | None = None):
+def attn_fwd_qk_materialised(q, k, v, causal: bool, scale: float | None = None,
+                             align: str = "bottom_right"):
     """numpy fp64 twin of :func:`attn_fwd_qk` with the whole Nq x Nk score matrix."""
+    shift = {"bottom_right": None, "top_left": 0}[align]
     q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
     B, H, Nq, d = q64.shape
     Nk = k64.shape[2]
@@ -152,7 +160,7 @@ def attn_fwd_qk_materialised(q, k, v, causal: bool, scale: float | None = None):
     s = scale * np.einsum("bhid,bhjd->bhij", q64, k64)
     keep = np.ones((Nq, Nk), dtype=bool)
     if causal:
-        keep = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+        keep = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq if shift is None else shift)
     s = np.where(keep, s, -np.inf)
     m = s.max(axis=-1, keepdims=True)
     empty = ~np.isfinite(m)

@@ -36,8 +36,11 @@
  * the LAST Nq positions of the Nk-long sequence (a KV-cache decode step, the
  * extension named at the end of "Getting the kernel correct, then benchmarking
  * it honestly"): row i sees keys j <= i + Nk - Nq. With Nq = Nk this is the
- * top-left mask above. A row that sees no key (only when causal and Nq > Nk)
- * gets O = 0 and LSE = -inf.
+ * top-left mask above. causal = 2 keeps the top-left alignment for any Nq, Nk
+ * (row i sees keys j <= i, the k_pos <= q_pos test of the profile-driven
+ * FlashAttention-2 page, "Round 4 / Causal tile-skipping", whose kernel takes
+ * N_QUERIES and N_KEYS separately). A row that sees no key (only when causal and
+ * Nq > Nk, bottom-right) gets O = 0 and LSE = -inf.
  */
 #include <math.h>
 #include <stdint.h>
@@ -177,7 +180,7 @@ static void oracle_row_n(const double* qi, const double* K, const double* V, int
 }
 
 /* Nq query rows against Nk keys: q, o [BH][Nq][d]; k, v [BH][Nk][d]; lse [BH][Nq].
- * Causal: row i sees keys j <= i + Nk - Nq. */
+ * causal = 0: every key; 1: row i sees keys j <= i + Nk - Nq; 2: keys j <= i. */
 int oracle_attn_fwd_qk(const double* q, const double* k, const double* v, double* o,
                        double* lse, int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
                        double scale)
@@ -196,7 +199,8 @@ int oracle_attn_fwd_qk(const double* q, const double* k, const double* v, double
                 for (int64_t i = 0; i < Nq; ++i) {
                     int64_t n_vis = Nk;
                     if (causal) {
-                        const int64_t last = i + Nk - Nq;  /* last visible key */
+                        /* last visible key: bottom-right (1) or top-left (2) alignment */
+                        const int64_t last = causal == 2 ? i : i + Nk - Nq;
                         n_vis = last < 0 ? 0 : (last + 1 < Nk ? last + 1 : Nk);
                     }
                     oracle_row_n(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * d, d, n_vis,

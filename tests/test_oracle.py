@@ -310,6 +310,33 @@ def test_qk_reduces_to_square_and_last_row_sees_all():
         assert abs(lz[0, 0, i] - math.log(n_vis)) < 1e-14
 
 
+@pytest.mark.parametrize("Nq,Nk", [(1, 10), (5, 15), (40, 25), (300, 7), (64, 64)])
+def test_qk_top_left_matches_materialised(Nq, Nk):
+    g = np.random.default_rng(Nq * 7 + Nk)
+    q = g.standard_normal((1, 3, Nq, 16))
+    k = g.standard_normal((1, 3, Nk, 16))
+    v = g.standard_normal((1, 3, Nk, 16))
+    o, lse = oracle.attn_fwd_qk(q, k, v, True, 0.4, align="top_left")
+    o2, lse2 = oracle.attn_fwd_qk_materialised(q, k, v, True, 0.4, align="top_left")
+    np.testing.assert_allclose(o, o2, rtol=0, atol=TIGHT)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=TIGHT)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(3, 50), (50, 3), (17, 130)])
+def test_qk_top_left_matches_torch_is_causal(Nq, Nk):
+    """torch's SDPA with is_causal=True keeps the top-left alignment for Nq != Nk, so
+    it pins the top-left mode without spelling the mask out."""
+    q, _, _ = make_qkv(1, 2, Nq, 64, "fp16", seed=Nq + 5)
+    _, k, v = make_qkv(1, 2, Nk, 64, "fp16", seed=Nk + 6)
+    o, _ = oracle.attn_fwd_qk(q, k, v, True, 0.125, align="top_left")
+    q64, k64, v64 = (t.to(torch.float64) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(q64, k64, v64, is_causal=True, scale=0.125)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    # the two alignments differ whenever Nq != Nk
+    ob, _ = oracle.attn_fwd_qk(q, k, v, True, 0.125, align="bottom_right")
+    assert np.abs(ob - o).max() > 1e-3
+
+
 def test_qk_rows_without_keys():
     """More query rows than keys under the causal mask: the first Nq - Nk rows see no
     key and get O = 0, LSE = -inf; the others see keys up to their diagonal."""
