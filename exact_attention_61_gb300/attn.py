@@ -18,6 +18,12 @@ LIB_PATH = os.path.join(HERE, "libattn.so")
 ATTN_FP16 = 0
 ATTN_BF16 = 1
 
+ATTN_MASK_NONE = 0
+ATTN_MASK_CAUSAL = 1
+ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2
+MASKS = {"none": ATTN_MASK_NONE, "causal": ATTN_MASK_CAUSAL,
+         "causal_bottom_right": ATTN_MASK_CAUSAL_BOTTOM_RIGHT}
+
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
 ATTN_ERR_UNSUPPORTED = 2
@@ -31,6 +37,12 @@ _lib = None
 _FWD_ARGS = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
              ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
+
+
+_FWD_KV_ARGS = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                ctypes.c_void_p]
 
 
 class AttnError(RuntimeError):
@@ -53,6 +65,12 @@ def load(path: str = LIB_PATH):
             lib.attn_fwd.restype = ctypes.c_int
             lib.attn_fwd_checked.argtypes = _FWD_ARGS
             lib.attn_fwd_checked.restype = ctypes.c_int
+            lib.attn_fwd_kv.argtypes = _FWD_KV_ARGS
+            lib.attn_fwd_kv.restype = ctypes.c_int
+            lib.attn_fwd_kv_checked.argtypes = _FWD_KV_ARGS
+            lib.attn_fwd_kv_checked.restype = ctypes.c_int
+            lib.attn_fwd_kv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
+            lib.attn_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_strerror.argtypes = [ctypes.c_int]
             lib.attn_strerror.restype = ctypes.c_char_p
             lib.attn_last_cuda_error.argtypes = []
@@ -103,6 +121,20 @@ def attn_fwd_checked(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream) 
                                        float(scale), int(dtype), stream))
 
 
+def attn_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, workspace, workspace_bytes,
+                stream, checked: bool = False) -> int:
+    """Raw C call of attn_fwd_kv (or attn_fwd_kv_checked); returns the attn_status_t."""
+    lib = load()
+    fn = lib.attn_fwd_kv_checked if checked else lib.attn_fwd_kv
+    return int(fn(q, k, v, o, lse, B, H, Nq, Nk, d, int(mask), float(scale), int(dtype), workspace,
+                  int(workspace_bytes), stream))
+
+
+def workspace_bytes(B, H, Nq, Nk, d) -> int:
+    """Workspace size for attn_fwd_kv's full split of the keys (0: never splits)."""
+    return int(load().attn_fwd_kv_workspace_bytes(B, H, Nq, Nk, d))
+
+
 def _dtype_code(t) -> int:
     import torch
     if t.dtype == torch.float16:
@@ -143,6 +175,49 @@ def fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, 
     st = call(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N,
               d, causal, scale, _dtype_code(q), stream.cuda_stream)
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def fwd_kv(q, k, v, mask: str = "none", scale: Optional[float] = None, out=None, lse=None,
+           workspace=None, stream=None, checked: bool = False) -> Tuple[object, object]:
+    """Attention forward of q [B, H, Nq, d] against k, v [B, H, Nk, d] (CUDA, fp16/bf16,
+    contiguous), e.g. one KV-cache decode step.
+
+    ``mask`` is "none", "causal" (row i sees keys j <= i) or "causal_bottom_right"
+    (row i sees keys j <= i + Nk - Nq). ``workspace`` is a CUDA uint8 tensor for the
+    split of the keys; by default one of :func:`workspace_bytes` bytes is allocated
+    here (pass ``workspace=False`` for none). Returns (o like q, lse fp32 [B, H, Nq]).
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] must agree on B, H and d")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if mask not in MASKS:
+        raise ValueError(f"mask must be one of {sorted(MASKS)}")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = workspace_bytes(B, H, Nq, Nk, d)
+        workspace = torch.empty((n,), dtype=torch.uint8, device=q.device) if n else False
+    ws_ptr, ws_n = (workspace.data_ptr(), workspace.numel()) if workspace is not False else (None, 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                     Nq, Nk, d, MASKS[mask], scale, _dtype_code(q), ws_ptr, ws_n, stream.cuda_stream,
+                     checked=checked)
+    _check(st, "attn_fwd_kv")
     return out, lse
 
 

@@ -4,6 +4,7 @@ Translation units (compiled in parallel, then linked into one shared library
 with the CUDA runtime linked statically):
   attn_host.cu                       C ABI, validation, tensor maps, dispatch
   probe.cu                           one-tile tensor-core probe (test hook)
+  attn_merge.cu                      merge of split-key partials
   attn_fwd_inst.cu x 4               forward kernel, one unit per (d, dtype)
 """
 from __future__ import annotations
@@ -28,6 +29,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxe
 UNITS = [
     ("attn_host.cu", [], "attn_host.o"),
     ("probe.cu", [], "probe.o"),
+    ("attn_merge.cu", [], "attn_merge.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=0"], "attn_fwd_d64_f16.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=1"], "attn_fwd_d64_bf16.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=128", "-DATTN_INST_BF16=0"], "attn_fwd_d128_f16.o"),

@@ -1,4 +1,5 @@
-// One (head dimension, dtype) pair of forward-kernel instances, causal and not.
+// One (head dimension, dtype) pair of forward-kernel instances: causal or not, whole
+// key range or split of the keys.
 // Compiled once per pair with -DATTN_INST_D=<64|128> -DATTN_INST_BF16=<0|1>.
 #include <atomic>
 
@@ -12,10 +13,10 @@
 namespace attn_sm103 {
 namespace {
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPLIT>
 cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s) {
     using C = FwdCfg<D>;
-    auto* kern = attn_fwd_kernel<D, CAUSAL, BF16>;
+    auto* kern = attn_fwd_kernel<D, CAUSAL, BF16, SPLIT>;
     // The dynamic shared-memory opt-in is per device; remember which devices have it.
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -27,7 +28,8 @@ cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s)
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const unsigned grid = static_cast<unsigned>(p.n_ctiles) * static_cast<unsigned>(p.BH);
+    const dim3 grid(static_cast<unsigned>(p.n_ctiles) * static_cast<unsigned>(p.BH),
+                    SPLIT ? static_cast<unsigned>(p.n_splits) : 1u);
     kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], p);
     return cudaGetLastError();
 }
@@ -43,9 +45,14 @@ cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s)
 #endif
 #define ATTN_LAUNCH_NAME ATTN_CAT(ATTN_CAT(ATTN_CAT(launch_fwd_d, ATTN_INST_D), _), ATTN_DT_SUFFIX)
 
-cudaError_t ATTN_LAUNCH_NAME(bool causal, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s) {
-    return causal ? launch_one<ATTN_INST_D, true, ATTN_INST_BF16 != 0>(maps, p, s)
-                  : launch_one<ATTN_INST_D, false, ATTN_INST_BF16 != 0>(maps, p, s);
+cudaError_t ATTN_LAUNCH_NAME(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p,
+                             cudaStream_t s) {
+    constexpr bool kBf16 = ATTN_INST_BF16 != 0;
+    if (split)
+        return causal ? launch_one<ATTN_INST_D, true, kBf16, true>(maps, p, s)
+                      : launch_one<ATTN_INST_D, false, kBf16, true>(maps, p, s);
+    return causal ? launch_one<ATTN_INST_D, true, kBf16, false>(maps, p, s)
+                  : launch_one<ATTN_INST_D, false, kBf16, false>(maps, p, s);
 }
 
 }  // namespace attn_sm103

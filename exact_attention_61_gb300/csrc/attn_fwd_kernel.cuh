@@ -215,7 +215,9 @@ __device__ __forceinline__ float row_max128(const uint32_t (&sr)[4][32]) {
     return fmaxf(fmax3(acc[0], acc[1], acc[2]), fmax3(fmax3(acc[3], acc[4], acc[5]), acc[6], acc[7]));
 }
 
-template <int D, bool CAUSAL, bool BF16>
+// SPLIT: this CTA covers key tiles [blockIdx.y * tiles_per_split, ...) only and writes
+// fp32 partials (O_s = O/l and log2-sum-exp) instead of O and LSE.
+template <int D, bool CAUSAL, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -238,13 +240,30 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     // ---- which rows this CTA owns (heaviest causal tiles are launched first) --------
     const int bh = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.BH));
     const int ct = p.n_ctiles - 1 - static_cast<int>(blockIdx.x / static_cast<uint32_t>(p.BH));
-    const int N = p.N;
-    const int n_kv_all = (N + C::BN - 1) / C::BN;
+    const int Nq = p.Nq, Nk = p.Nk;
+    // Under the causal mask row i sees keys j <= i + off: off = 0 aligns the first query
+    // row with the first key (top-left), off = Nk - Nq makes the query rows the last Nq
+    // positions of the key sequence (bottom-right, as in decoding).
+    const int off = p.causal_off;
+    const int n_kv_all = (Nk + C::BN - 1) / C::BN;
+    const int kv_begin = SPLIT ? static_cast<int>(blockIdx.y) * p.tiles_per_split : 0;
+    const int kv_end = SPLIT ? min(n_kv_all, kv_begin + p.tiles_per_split) : n_kv_all;
     // First query row and number of key tiles of each Q tile (kept in scalars: an
     // array indexed by the tile would live in local memory).
+    // Key tiles a Q tile needs: all of [kv_begin, kv_end), or, under the causal mask,
+    // those up to the one holding the last visible key of its last row.
+    auto tiles_for = [&](int r0) -> int {
+        if (r0 >= Nq) return 0;
+        int end = n_kv_all;
+        if (CAUSAL) {
+            const int last_key = min(r0 + C::BM - 1, Nq - 1) + off;
+            end = last_key < 0 ? 0 : min(n_kv_all, last_key / C::BN + 1);
+        }
+        return max(0, min(end, kv_end) - kv_begin);
+    };
     const int row0_0 = ct * C::kRowsPerCta, row0_1 = row0_0 + C::BM;
-    const int nkv_0 = CAUSAL ? min(n_kv_all, row0_0 / C::BN + 1) : n_kv_all;
-    const int nkv_1 = row0_1 < N ? (CAUSAL ? min(n_kv_all, row0_1 / C::BN + 1) : n_kv_all) : 0;
+    const int nkv_0 = tiles_for(row0_0);
+    const int nkv_1 = tiles_for(row0_1);
     auto row0 = [&](int t) { return t ? row0_1 : row0_0; };
     auto n_kv = [&](int t) { return t ? nkv_1 : nkv_0; };
     const int n_max = max(nkv_0, nkv_1);
@@ -294,11 +313,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d_hint(sK(s) + c * C::kBoxBytes, &tmK, bar(C::kBarKFull + s), c * 64,
-                                     j * C::BN, bh, pol_kv);
+                                     (kv_begin + j) * C::BN, bh, pol_kv);
                 mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d_hint(sV(s) + c * C::kBoxBytes, &tmV, bar(C::kBarVFull + s), c * 64,
-                                     j * C::BN, bh, pol_kv);
+                                     (kv_begin + j) * C::BN, bh, pol_kv);
                 issued = j + 1;
             }
             // Drain: every copy issued into this CTA's shared memory has landed before
@@ -392,7 +411,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const float2 qk2 = make_float2(qk, qk);
 
         bool ok = n_kv(t) > 0;
-        const bool single_tile = nkv_1 == 0;
+        // Only one Q tile has key tiles (the second is past the last row, or, with the
+        // bottom-right mask, the first sees no key): its jobs are consecutive.
+        const bool single_tile = nkv_0 == 0 || nkv_1 == 0;
+        // Warps whose 32 rows are all past the last query row (few query rows, as in
+        // decoding) skip the softmax arithmetic; their rows of O are never stored.
+        const bool warp_has_rows = row0(t) + static_cast<int>(wq * 32u) < Nq;
         float m = -INFINITY;  // running max, log2 units of the scaled scores (possibly stale)
         float l = 0.f;        // running sum of P (fp32), relative to m
         for (int j = 0; j < n_kv(t) && ok; ++j) {
@@ -404,6 +428,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
+            if (!warp_has_rows) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarPFull + b));
+                continue;
+            }
             uint32_t sr[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
@@ -411,10 +440,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
 
-            const int k0 = j * C::BN;
-            const bool need_mask = (k0 + C::BN > N) || (CAUSAL && k0 + C::BN - 1 > row0(t));
+            const int k0 = (kv_begin + j) * C::BN;
+            const bool need_mask = (k0 + C::BN > Nk) || (CAUSAL && k0 + C::BN - 1 > row0(t) + off);
             if (need_mask) {
-                const int lim = CAUSAL ? min(N, q_row + 1) : N;  // keys [k0, lim) are visible
+                const int lim = CAUSAL ? min(Nk, q_row + off + 1) : Nk;  // keys below lim are visible
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -485,46 +514,87 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             if (lane == 0) mbar_arrive(bar(C::kBarPFull + b));
         }
 
-        // ---- epilogue: O / l -> dtype -> swizzled SMEM (reusing this Q tile) -> TMA store
+        // ---- epilogue -----------------------------------------------------------------
+        // A row with no visible key (possible only with causal Nq > Nk, or in a split of
+        // the keys) has l = 0: its output is O = 0 and LSE = -inf.
         if (ok) {
             // o_final completes once, after the last O += P V of this tile.
             ok = wait_warp(bar(C::kBarOFinal + t), 0, wc, role * 1000 + C::kBarOFinal + t, n_kv(t));
         }
-        if (ok) {
-            tc_fence_after_sync();
-            const float inv_l = 1.f / l;
-            uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;
+        const float m_fin = (m == -INFINITY) ? 0.f : m;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float lse2 = l > 0.f ? m_fin + log2f(l) : -INFINITY;  // log2 units
+        if constexpr (SPLIT) {
+            // fp32 partials for the merge: O_s = O / l and log2-sum-exp of this key range.
+            const bool valid_tile = row0(t) < Nq;
+            if (valid_tile && warp_has_rows && (n_kv(t) == 0 || ok)) {
+                const size_t prow = (static_cast<size_t>(bh) * p.n_splits + blockIdx.y) * Nq + q_row;
+                float* dst = p.o_part + prow * D;
+                if (n_kv(t) > 0) tc_fence_after_sync();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
-                tmem_ld_wait();
-                reg_fence(o);
-                uint32_t h[16];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    if (n_kv(t) > 0) {
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+                    }
+                    if (q_row < Nq) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    h[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-                const int box = c >> 1;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t chunk = (c & 1) * 4 + i;
-                    uint4 v = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-                    *reinterpret_cast<uint4*>(stage + box * C::kBoxBytes + sw128_offset(r, chunk)) = v;
+                        for (int e = 0; e < 32; e += 4) {
+                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (n_kv(t) > 0)
+                                v = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
+                                                __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+                            *reinterpret_cast<float4*>(dst + c * 32 + e) = v;
+                        }
+                    }
                 }
+                if (q_row < Nq) p.lse_part[prow] = n_kv(t) > 0 ? lse2 : -INFINITY;
             }
-            if (q_row < N) {
-                const float m_fin = (m == -INFINITY) ? 0.f : m;
-                p.lse[static_cast<size_t>(bh) * N + q_row] = (m_fin + log2f(l)) * 0.69314718055994530942f;
+        } else {
+            // O / l -> dtype -> swizzled SMEM (reusing this Q tile) -> TMA store. A tile
+            // that sees no key at all stores zeros (its Q was never loaded).
+            const bool valid_tile = row0(t) < Nq;
+            const bool has_kv = n_kv(t) > 0;
+            if ((ok || !has_kv) && valid_tile && warp_has_rows) {
+                if (has_kv) tc_fence_after_sync();
+                uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    if (has_kv) {
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
+                    uint32_t h[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        h[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+                    const int box = c >> 1;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t chunk = (c & 1) * 4 + i;
+                        uint4 v = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                        *reinterpret_cast<uint4*>(stage + box * C::kBoxBytes + sw128_offset(r, chunk)) = v;
+                    }
+                }
+                if (q_row < Nq)
+                    p.lse[static_cast<size_t>(bh) * Nq + q_row] = lse2 * 0.69314718055994530942f;
             }
-        }
-        fence_proxy_async_smem();
-        if (n_kv(t) > 0) named_bar_sync(1 + t, 128);
-        if (n_kv(t) > 0 && wq == 0 && lane == 0 && *wc.abort == 0u) {
-            tma_prefetch_desc(&tmO);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_store_3d(&tmO, sQ(t) + c * C::kBoxBytes, c * 64, row0(t), bh);
-            tma_store_commit();
-            tma_store_wait_all();
+            fence_proxy_async_smem();
+            if (valid_tile) named_bar_sync(1 + t, 128);
+            if (valid_tile && wq == 0 && lane == 0 && *wc.abort == 0u) {
+                tma_prefetch_desc(&tmO);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_store_3d(&tmO, sQ(t) + c * C::kBoxBytes, c * 64, row0(t), bh);
+                tma_store_commit();
+                tma_store_wait_all();
+            }
         }
     }
 
@@ -534,6 +604,45 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+}
+
+// Merge of split partials: per (b, h, query row), with log2-sum-exp values x_s of the
+// splits, X = max_s x_s, w_s = 2^(x_s - X), O = sum_s w_s O_s / sum_s w_s and
+// LSE = (X + log2 sum_s w_s) ln 2. One warp per row; lanes cover the head dimension.
+template <bool BF16>
+__global__ void __launch_bounds__(128) attn_merge_kernel(const MergeParams p) {
+    const int warp_global = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31u);
+    if (warp_global >= p.BH * p.Nq) return;
+    const int bh = warp_global / p.Nq, i = warp_global % p.Nq;
+    const float* lp = p.lse_part + static_cast<size_t>(bh) * p.n_splits * p.Nq + i;
+    float X = -INFINITY;
+    for (int s = 0; s < p.n_splits; ++s) X = fmaxf(X, lp[static_cast<size_t>(s) * p.Nq]);
+    const int per_lane = p.d / 32;  // 2 or 4
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.f;
+    if (X != -INFINITY) {
+        for (int s = 0; s < p.n_splits; ++s) {
+            const float x = lp[static_cast<size_t>(s) * p.Nq];
+            if (x == -INFINITY) continue;
+            const float w = ex2_ftz(x - X);
+            wsum += w;
+            const float* op = p.o_part + ((static_cast<size_t>(bh) * p.n_splits + s) * p.Nq + i) * p.d;
+            for (int e = 0; e < per_lane; ++e) acc[e] += w * op[lane * per_lane + e];
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const size_t orow = (static_cast<size_t>(bh) * p.Nq + i) * p.d + lane * per_lane;
+    if constexpr (BF16) {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
+        for (int e = 0; e < per_lane; ++e) o[orow + e] = __float2bfloat16_rn(acc[e] * inv);
+    } else {
+        __half* o = static_cast<__half*>(p.o);
+        for (int e = 0; e < per_lane; ++e) o[orow + e] = __float2half_rn(acc[e] * inv);
+    }
+    if (lane == 0)
+        p.lse[static_cast<size_t>(bh) * p.Nq + i] =
+            wsum > 0.f ? (X + log2f(wsum)) * 0.69314718055994530942f : -INFINITY;
 }
 
 }  // namespace attn_sm103

@@ -1,6 +1,8 @@
 // C ABI of the attention forward (see include/attn.h): argument validation,
 // tensor-map encoding, device status record and dispatch to the kernel instances.
+#include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -67,35 +69,41 @@ bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
     return a0 < b0 + nb && b0 < a0 + na;
 }
 
-int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype) {
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int64_t B,
+             int64_t H, int64_t Nq, int64_t Nk, int64_t d, int mask, float scale, int dtype, const void* ws,
+             size_t ws_bytes) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (mask < ATTN_MASK_NONE || mask > ATTN_MASK_CAUSAL_BOTTOM_RIGHT) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    const uintptr_t ptrs[5] = {reinterpret_cast<uintptr_t>(q), reinterpret_cast<uintptr_t>(k),
+    const uintptr_t ptrs[6] = {reinterpret_cast<uintptr_t>(q), reinterpret_cast<uintptr_t>(k),
                                reinterpret_cast<uintptr_t>(v), reinterpret_cast<uintptr_t>(o),
-                               reinterpret_cast<uintptr_t>(lse)};
+                               reinterpret_cast<uintptr_t>(lse), reinterpret_cast<uintptr_t>(ws)};
     for (uintptr_t p : ptrs)
         if (p % 16u) return ATTN_ERR_MISALIGNED;
     const int64_t lim31 = (int64_t(1) << 31) - 1;
-    if (B > lim31 || H > lim31 || N > lim31) return ATTN_ERR_UNSUPPORTED;
+    if (B > lim31 || H > lim31 || Nq > lim31 || Nk > lim31) return ATTN_ERR_UNSUPPORTED;
     if (B * H > lim31) return ATTN_ERR_UNSUPPORTED;
     const int64_t BH = B * H;
-    if (BH > (int64_t(1) << 62) / (N * d)) return ATTN_ERR_UNSUPPORTED;
-    const int64_t n_ctiles = (N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
+    if (BH > (int64_t(1) << 62) / (Nq * d) || BH > (int64_t(1) << 62) / (Nk * d)) return ATTN_ERR_UNSUPPORTED;
+    const int64_t n_ctiles = (Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
     if (n_ctiles * BH > lim31) return ATTN_ERR_UNSUPPORTED;
-    const uint64_t tensor_bytes = static_cast<uint64_t>(BH * N * d) * 2u;
-    const uint64_t lse_bytes = static_cast<uint64_t>(BH * N) * 4u;
-    if (ranges_overlap(o, tensor_bytes, q, tensor_bytes) ||
-        ranges_overlap(o, tensor_bytes, k, tensor_bytes) ||
-        ranges_overlap(o, tensor_bytes, v, tensor_bytes) ||
-        ranges_overlap(o, tensor_bytes, lse, lse_bytes) ||
-        ranges_overlap(lse, lse_bytes, q, tensor_bytes) ||
-        ranges_overlap(lse, lse_bytes, k, tensor_bytes) ||
-        ranges_overlap(lse, lse_bytes, v, tensor_bytes))
+    const uint64_t q_bytes = static_cast<uint64_t>(BH * Nq * d) * 2u;
+    const uint64_t kv_bytes = static_cast<uint64_t>(BH * Nk * d) * 2u;
+    const uint64_t lse_bytes = static_cast<uint64_t>(BH * Nq) * 4u;
+    if (ranges_overlap(o, q_bytes, q, q_bytes) || ranges_overlap(o, q_bytes, k, kv_bytes) ||
+        ranges_overlap(o, q_bytes, v, kv_bytes) || ranges_overlap(o, q_bytes, lse, lse_bytes) ||
+        ranges_overlap(lse, lse_bytes, q, q_bytes) || ranges_overlap(lse, lse_bytes, k, kv_bytes) ||
+        ranges_overlap(lse, lse_bytes, v, kv_bytes))
         return ATTN_ERR_INVALID_ARG;
+    if (ws && ws_bytes) {
+        const void* all[5] = {q, k, v, o, lse};
+        const uint64_t sz[5] = {q_bytes, kv_bytes, kv_bytes, q_bytes, lse_bytes};
+        for (int i = 0; i < 5; ++i)
+            if (ranges_overlap(ws, ws_bytes, all[i], sz[i])) return ATTN_ERR_INVALID_ARG;
+    }
     return ATTN_OK;
 }
 
@@ -134,11 +142,42 @@ cudaError_t select_device_of(const void* ptr, int* dev_out) {
     return cudaSuccess;
 }
 
+// Split of the keys over CTAs for few query rows (decoding): aim for two CTAs per SM
+// of a 152-SM GB300, at least one key tile per split, limited by the workspace.
+constexpr int64_t kSplitTargetCtas = 2 * 152;
+
+SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes) {
+    SplitPlan pl{1, 0, 0, 0};
+    const int64_t n_kv_all = (Nk + 127) / 128;
+    pl.tiles_per_split = n_kv_all;
+    const int64_t ctas = ((Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta) * BH;
+    if (ctas >= kSplitTargetCtas) return pl;  // enough CTAs already
+    int64_t want = (kSplitTargetCtas + ctas - 1) / ctas;
+    want = std::min<int64_t>(std::min<int64_t>(want, n_kv_all), 65535);
+    if (want <= 1) return pl;
+    const uint64_t per_split = static_cast<uint64_t>(BH) * Nq * (d + 1) * 4u;
+    const int64_t fit = static_cast<int64_t>(ws_bytes / per_split);
+    const int64_t n = std::min(want, fit);
+    if (n <= 1) return pl;
+    const int64_t tps = (n_kv_all + n - 1) / n;
+    pl.tiles_per_split = tps;
+    pl.n_splits = (n_kv_all + tps - 1) / tps;
+    if (pl.n_splits <= 1) {
+        pl.n_splits = 1;
+        pl.tiles_per_split = n_kv_all;
+        return pl;
+    }
+    pl.o_part_bytes = static_cast<uint64_t>(BH) * pl.n_splits * Nq * d * 4u;
+    pl.bytes = pl.o_part_bytes + static_cast<uint64_t>(BH) * pl.n_splits * Nq * 4u;
+    return pl;
+}
+
 namespace {
 
-int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-             int64_t N, int64_t d, int causal, float scale, int dtype, void* stream, uint32_t** status_out) {
-    const int st = validate(q, k, v, o, lse, B, H, N, d, scale, dtype);
+int fwd_kv_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                int64_t Nq, int64_t Nk, int64_t d, int mask, float scale, int dtype, void* ws,
+                size_t ws_bytes, void* stream) {
+    const int st = validate(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, ws, ws_bytes);
     if (st != ATTN_OK) return st;
     int dev = 0;
     cudaError_t e = select_device_of(q, &dev);
@@ -148,13 +187,14 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (!enc) return cuda_fail(e);
     uint32_t* status = status_ptr(dev, &e);
     if (!status) return cuda_fail(e);
-    if (status_out) *status_out = status;
 
     const int64_t BH = B * H;
+    const SplitPlan plan = plan_split(BH, Nq, Nk, d, ws ? ws_bytes : 0);
     alignas(64) CUtensorMap maps[4];
     const void* ptrs[4] = {q, k, v, o};
+    const int64_t rows[4] = {Nq, Nk, Nk, Nq};
     for (int i = 0; i < 4; ++i) {
-        const CUresult r = make_map(enc, &maps[i], ptrs[i], BH, N, d, dtype);
+        const CUresult r = make_map(enc, &maps[i], ptrs[i], BH, rows[i], d, dtype);
         if (r != CUDA_SUCCESS) {
             g_last_cuda_error = 100000 + static_cast<int>(r);
             return ATTN_ERR_CUDA;
@@ -163,18 +203,68 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     FwdParams p;
     p.lse = lse;
     p.err = status;
-    p.N = static_cast<int>(N);
+    p.Nq = static_cast<int>(Nq);
+    p.Nk = static_cast<int>(Nk);
     p.BH = static_cast<int>(BH);
-    p.n_ctiles = static_cast<int>((N + kFwdRowsPerCta - 1) / kFwdRowsPerCta);
+    p.n_ctiles = static_cast<int>((Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta);
     p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.causal_off = mask == ATTN_MASK_CAUSAL_BOTTOM_RIGHT ? static_cast<int>(Nk - Nq) : 0;
+    p.n_splits = static_cast<int>(plan.n_splits);
+    p.tiles_per_split = static_cast<int>(plan.tiles_per_split);
+    const bool split = plan.n_splits > 1;
+    p.o_part = split ? static_cast<float*>(ws) : nullptr;
+    p.lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.o_part_bytes) : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool c = causal != 0;
+    const bool c = mask != ATTN_MASK_NONE;
     if (d == 64)
-        e = dtype == ATTN_BF16 ? launch_fwd_d64_bf16(c, maps, p, s) : launch_fwd_d64_f16(c, maps, p, s);
+        e = dtype == ATTN_BF16 ? launch_fwd_d64_bf16(c, split, maps, p, s) : launch_fwd_d64_f16(c, split, maps, p, s);
     else
-        e = dtype == ATTN_BF16 ? launch_fwd_d128_bf16(c, maps, p, s) : launch_fwd_d128_f16(c, maps, p, s);
+        e = dtype == ATTN_BF16 ? launch_fwd_d128_bf16(c, split, maps, p, s) : launch_fwd_d128_f16(c, split, maps, p, s);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (split) {
+        MergeParams mp{p.o_part, p.lse_part, o, lse, p.BH, p.Nq, static_cast<int>(d), p.n_splits};
+        e = launch_merge(dtype == ATTN_BF16, mp, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     return ATTN_OK;
+}
+
+int checked(int (*run)(void*), void* ctx, const void* q, void* stream) {
+    int dev = 0;
+    cudaError_t e = select_device_of(q, &dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t* status = status_ptr(dev, &e);
+    if (!status) return cuda_fail(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int st = run(ctx);
+    if (st != ATTN_OK) return st;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t host[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(host, status, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return host[0] ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+struct KvArgs {
+    const void *q, *k, *v;
+    void* o;
+    float* lse;
+    int64_t B, H, Nq, Nk, d;
+    int mask;
+    float scale;
+    int dtype;
+    void* ws;
+    size_t ws_bytes;
+    void* stream;
+};
+
+int run_kv(void* ctx) {
+    const KvArgs* a = static_cast<const KvArgs*>(ctx);
+    return fwd_kv_impl(a->q, a->k, a->v, a->o, a->lse, a->B, a->H, a->Nq, a->Nk, a->d, a->mask, a->scale,
+                       a->dtype, a->ws, a->ws_bytes, a->stream);
 }
 
 }  // namespace
@@ -186,29 +276,39 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
              int64_t N, int64_t d, int causal, float scale, int dtype, void* stream) {
-    return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream, nullptr);
+    const int mask = causal ? ATTN_MASK_CAUSAL : ATTN_MASK_NONE;
+    return fwd_kv_impl(q, k, v, o, lse, B, H, N, N, d, mask, scale, dtype, nullptr, 0, stream);
 }
 
 int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                      int64_t H, int64_t N, int64_t d, int causal, float scale, int dtype, void* stream) {
-    int st = validate(q, k, v, o, lse, B, H, N, d, scale, dtype);
+    const int mask = causal ? ATTN_MASK_CAUSAL : ATTN_MASK_NONE;
+    const int st = validate(q, k, v, o, lse, B, H, N, N, d, mask, scale, dtype, nullptr, 0);
     if (st != ATTN_OK) return st;
-    int dev = 0;
-    cudaError_t e = select_device_of(q, &dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    uint32_t* status = status_ptr(dev, &e);
-    if (!status) return cuda_fail(e);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    st = fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream, nullptr);
+    KvArgs a{q, k, v, o, lse, B, H, N, N, d, mask, scale, dtype, nullptr, 0, stream};
+    return checked(run_kv, &a, q, stream);
+}
+
+size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
+    if (B > INT32_MAX || H > INT32_MAX || Nq > INT32_MAX || Nk > INT32_MAX || B * H > INT32_MAX) return 0;
+    return static_cast<size_t>(plan_split(B * H, Nq, Nk, d, SIZE_MAX).bytes);
+}
+
+int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                int64_t Nq, int64_t Nk, int64_t d, int mask, float scale, int dtype, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    return fwd_kv_impl(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, workspace, workspace_bytes,
+                       stream);
+}
+
+int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                        int64_t H, int64_t Nq, int64_t Nk, int64_t d, int mask, float scale, int dtype,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    const int st = validate(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, workspace, workspace_bytes);
     if (st != ATTN_OK) return st;
-    e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    uint32_t host[4] = {0, 0, 0, 0};
-    e = cudaMemcpy(host, status, sizeof(host), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return host[0] ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    KvArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, workspace, workspace_bytes, stream};
+    return checked(run_kv, &a, q, stream);
 }
 
 const char* attn_strerror(int status) {

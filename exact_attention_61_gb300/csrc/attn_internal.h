@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI host code and the kernel instances.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -10,12 +11,27 @@ namespace attn_sm103 {
 
 // Scalar arguments of the forward kernel (the four tensor maps are passed beside it).
 struct FwdParams {
-    float* lse;      // [BH, N] fp32, natural-log logsumexp of the scaled scores
-    uint32_t* err;   // device status record {code, block, where, iteration}
-    int N;           // sequence length (queries = keys)
-    int BH;          // batch * heads
-    int n_ctiles;    // ceil(N / 256): CTA tiles per head
-    float qk_scale;  // scale * log2(e), > 0
+    float* lse;       // [BH, Nq] fp32, natural-log logsumexp of the scaled scores
+    uint32_t* err;    // device status record {code, block, where, iteration}
+    int Nq;           // query rows per head
+    int Nk;           // keys per head
+    int BH;           // batch * heads
+    int n_ctiles;     // ceil(Nq / 256): CTA tiles per head
+    float qk_scale;   // scale * log2(e), > 0
+    int causal_off;   // causal kernels: row i sees keys j <= i + causal_off
+    int tiles_per_split;  // key tiles per split (split s covers tiles [s*tps, (s+1)*tps))
+    int n_splits;         // gridDim.y
+    float* o_part;    // split mode: [BH][n_splits][Nq][d] fp32 partial outputs (O_s = O/l)
+    float* lse_part;  // split mode: [BH][n_splits][Nq] fp32 partial log2-sum-exp (-inf if empty)
+};
+
+// Merge of split partials into O (dtype) and LSE (natural log).
+struct MergeParams {
+    const float* o_part;
+    const float* lse_part;
+    void* o;
+    float* lse;
+    int BH, Nq, d, n_splits;
 };
 
 // Query rows one CTA of the forward kernel owns.
@@ -24,10 +40,20 @@ constexpr int kFwdRowsPerCta = 256;
 // Enqueue one forward launch. maps = {Q, K, V, O} tensor maps (3-D: d, N, B*H;
 // 64 x 128 boxes, 128-byte swizzle). Implemented once per (d, dtype) in
 // attn_fwd_inst.cu; `causal` picks the template instance.
-cudaError_t launch_fwd_d64_f16(bool causal, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
-cudaError_t launch_fwd_d64_bf16(bool causal, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
-cudaError_t launch_fwd_d128_f16(bool causal, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
-cudaError_t launch_fwd_d128_bf16(bool causal, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
+// `split` selects the instance that writes fp32 partials (p.n_splits > 1); the
+// grid is (n_ctiles * BH, n_splits).
+cudaError_t launch_fwd_d64_f16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_d64_bf16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_d128_f16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_d128_bf16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_merge(bool bf16, const MergeParams& p, cudaStream_t s);
+
+// How the keys are split over CTAs (n_splits = 1: no split, no workspace).
+struct SplitPlan {
+    int64_t n_splits, tiles_per_split;
+    uint64_t o_part_bytes, bytes;  // workspace: fp32 O partials, then fp32 LSE partials
+};
+SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes);
 
 // Host helpers shared by the C-ABI entry points (defined in attn_host.cu).
 int cuda_fail(cudaError_t e);  // records e for attn_last_cuda_error(); returns ATTN_ERR_CUDA

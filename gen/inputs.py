@@ -117,3 +117,50 @@ def make_qkv_rising(B: int, H: int, N: int, d: int, dtype: str, seed: int, step:
     k.add_(ramp.view(1, 1, N, 1))
     dt = to_dtype(dtype)
     return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
+
+
+def make_qkv_kv(B: int, H: int, Nq: int, Nk: int, d: int, dtype: str, seed: int,
+                input_scale: float = 1.0):
+    """Q [B, H, Nq, d] and K, V [B, H, Nk, d], i.i.d. N(0,1) (times ``input_scale``).
+
+    Same recipe as :func:`make_qkv` (one seeded generator, Q then K then V, fp32,
+    one round-to-nearest-even cast) with separate query and key lengths, as in a
+    KV-cache decode step (a few query rows against a long cache).
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    out = []
+    for n in (Nq, Nk, Nk):
+        x = torch.randn((B, H, n, d), generator=g, dtype=torch.float32)
+        if input_scale != 1.0:
+            x.mul_(input_scale)
+        out.append(x.to(to_dtype(dtype)).contiguous())
+    return tuple(out)
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One KV-cache decode problem: Nq new query rows against an Nk-long cache."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str
+    seed: int
+
+
+# Decode problems (the pages print no decode shapes; these are chosen to span a batch
+# of single-token steps, a long single-sequence cache and a few-token speculative step).
+DECODE_WORKLOADS: List[DecodeWorkload] = [
+    DecodeWorkload("b8h32q1k8192d128", 8, 32, 1, 8192, 128, "bf16", 61100),
+    DecodeWorkload("b1h16q1k65536d128", 1, 16, 1, 65536, 128, "bf16", 61101),
+    DecodeWorkload("b16h16q4k4096d64", 16, 16, 4, 4096, 64, "fp16", 61102),
+]
+
+
+def decode_workload(name: str) -> DecodeWorkload:
+    for w in DECODE_WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)

@@ -42,6 +42,7 @@
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -52,6 +53,14 @@ typedef enum {
     ATTN_FP16 = 0,
     ATTN_BF16 = 1
 } attn_dtype_t;
+
+/* Mask of attn_fwd_kv (attn_fwd's `causal` != 0 is ATTN_MASK_CAUSAL). */
+typedef enum {
+    ATTN_MASK_NONE = 0,                /* every key                                     */
+    ATTN_MASK_CAUSAL = 1,              /* row i sees keys j <= i (top-left)             */
+    ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2  /* row i sees keys j <= i + Nk - Nq: the query
+                                          rows are the last Nq positions (decoding)    */
+} attn_mask_t;
 
 typedef enum {
     ATTN_OK = 0,
@@ -89,6 +98,56 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
                      int dtype, void* stream);
+
+/*
+ * attn_fwd_kv -- forward pass of Nq query rows against Nk keys, enqueued on
+ * `stream`: a KV-cache decode step (Nq small, Nk the cache length) or any other
+ * pair of lengths.
+ *
+ * Sources: "Programming an attention kernel in Triton", Kernel 4, runs queries
+ * against a longer key/value sequence (a single query against ten keys among its
+ * tests); the kernel of the profile-driven FlashAttention-2 page takes N_QUERIES
+ * and N_KEYS separately and masks k_pos <= q_pos ("Round 4 / Causal
+ * tile-skipping"), which is ATTN_MASK_CAUSAL; "Getting the kernel correct, then
+ * benchmarking it honestly" names KV-cache decode as the next extension, whose
+ * new query rows are the last positions of the sequence:
+ * ATTN_MASK_CAUSAL_BOTTOM_RIGHT.
+ *
+ *  - q, o: DEVICE [B, H, Nq, d] of `dtype`; k, v: DEVICE [B, H, Nk, d] of
+ *    `dtype`; lse: DEVICE [B, H, Nq] fp32. Alignment, overlap and size rules
+ *    as above, with Nq and Nk in place of N.
+ *  - mask: an attn_mask_t; anything else is ATTN_ERR_INVALID_ARG. A row that
+ *    sees no key (bottom-right with Nq > Nk) gets O = 0 and LSE = -inf.
+ *  - workspace: optional DEVICE scratch owned by the caller (16-byte aligned,
+ *    not overlapping the other arrays; NULL or 0 bytes allowed). When the
+ *    query rows alone give too few CTAs for the GPU, the keys are split into
+ *    ranges processed by separate CTAs whose fp32 partial outputs and
+ *    log-sum-exps go to the workspace and are merged by a second kernel on the
+ *    same stream; how many ranges is bounded by workspace_bytes, and with too
+ *    little workspace the call runs unsplit (same results up to fp32
+ *    rounding order, fewer CTAs). Nothing in it needs to be initialised; it
+ *    is read and written only by the kernels of this call, so calls that may
+ *    run at the same time need workspaces of their own. The split of the
+ *    keys has no counterpart in the pages: it is this library's way of
+ *    filling the GPU when Nq is small.
+ *  - Returns as attn_fwd.
+ */
+int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
+                int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int mask,
+                float scale, int dtype, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* attn_fwd_kv_checked -- attn_fwd_kv, then synchronise and read the device
+ * status word, as attn_fwd_checked. */
+int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int mask,
+                        float scale, int dtype, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* attn_fwd_kv_workspace_bytes -- the workspace size with which attn_fwd_kv uses
+ * its full split of the keys for these sizes (0: it never splits them). Pure
+ * host arithmetic, no CUDA call; 0 for sizes attn_fwd_kv rejects. */
+size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d);
 
 /* attn_strerror -- static, human-readable text for an attn_status_t. Never NULL. */
 const char* attn_strerror(int status);

@@ -89,3 +89,68 @@ def test_probe_validation(lib):
     assert f(A, A, A, A, A, A, 96, 1, None) == 2
     assert f(A, A, A, A + 4, A, A, 64, 1, None) == 3
     assert f(A, A, A, A, A, A, 64, 7, None) == 1
+
+
+def test_headers_declare_the_kv_forward():
+    names = _declared_symbols()
+    for n in ("attn_fwd_kv", "attn_fwd_kv_checked", "attn_fwd_kv_workspace_bytes"):
+        assert n in names
+
+
+def _call_kv(lib_mod, checked=False, **kw):
+    args = dict(q=A, k=2 * A * 64, v=3 * A * 64, o=4 * A * 64, lse=5 * A * 64, B=1, H=2, Nq=4,
+                Nk=1000, d=64, mask=2, scale=0.125, dtype=1, workspace=None, workspace_bytes=0,
+                stream=None)
+    args.update(kw)
+    return lib_mod.attn_fwd_kv(**args, checked=checked)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), 1), (dict(Nq=0), 1), (dict(Nk=0), 1), (dict(Nk=-1), 1),
+    (dict(mask=3), 1), (dict(mask=-1), 1), (dict(dtype=5), 1), (dict(scale=0.0), 1),
+    (dict(d=80), 2), (dict(Nk=1 << 31), 2),
+    (dict(k=2 * A * 64 + 8), 3), (dict(workspace=6 * A * 64 + 4, workspace_bytes=4096), 3),
+    (dict(workspace=A, workspace_bytes=4096), 1),               # workspace overlaps q
+    (dict(workspace=3 * A * 64 + 256, workspace_bytes=64), 1),  # workspace inside v
+    (dict(o=2 * A * 64), 1),                                     # o aliases k
+])
+def test_kv_host_validation(lib, kw, status):
+    from exact_attention_61_gb300 import attn
+    assert _call_kv(attn, **kw) == status
+    assert _call_kv(attn, checked=True, **kw) == status
+
+
+def _splits(attn, B, H, Nq, Nk, d):
+    n = attn.workspace_bytes(B, H, Nq, Nk, d)
+    per = B * H * Nq * (d + 1) * 4
+    assert n % per == 0
+    return n // per
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d", [
+    (1, 8, 1, 8192, 128), (8, 32, 1, 32768, 64), (1, 1, 1, 128, 64), (1, 1, 1, 129, 64),
+    (2, 4, 16, 65536, 128), (1, 16, 300, 20000, 64), (4, 16, 4096, 4096, 64), (1, 1, 5, 100, 64),
+])
+def test_workspace_split_plan(lib, B, H, Nq, Nk, d):
+    """The split of the keys: none when the query rows already give two CTAs per SM of
+    a 152-SM GPU or when there is a single key tile; else at least two non-empty ranges
+    of 128-key tiles, enough to reach that target when the keys allow."""
+    from exact_attention_61_gb300 import attn
+    ctas = -(-Nq // 256) * B * H
+    n_kv = -(-Nk // 128)
+    S = _splits(attn, B, H, Nq, Nk, d)
+    if ctas >= 304 or n_kv == 1:
+        assert S == 0
+        return
+    assert 2 <= S <= n_kv
+    tps = -(-n_kv // S)
+    assert (S - 1) * tps < n_kv <= S * tps  # no empty range
+    want = min(n_kv, -(-304 // ctas))
+    assert want / 2 <= S <= want  # whole tiles per range: at most a factor two below the target
+
+
+def test_workspace_bytes_rejects_bad_sizes(lib):
+    from exact_attention_61_gb300 import attn
+    assert attn.workspace_bytes(0, 1, 1, 100, 64) == 0
+    assert attn.workspace_bytes(1, 1, 1, 100, 96) == 0
+    assert attn.workspace_bytes(1, 1, 1, 0, 64) == 0
