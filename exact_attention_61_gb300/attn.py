@@ -30,6 +30,8 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_MISALIGNED = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_SCRATCH_TOO_SMALL = 6
+STATIC_SCRATCH_BYTES = 8 << 20  # scratch of attn_fwd_kv_static
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +73,8 @@ def load(path: str = LIB_PATH):
             lib.attn_fwd_kv_checked.restype = ctypes.c_int
             lib.attn_fwd_kv_workspace_bytes.argtypes = [ctypes.c_int64] * 5
             lib.attn_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_fwd_kv_static.argtypes = _FWD_KV_ARGS[:13] + [ctypes.c_void_p]
+            lib.attn_fwd_kv_static.restype = ctypes.c_int
             lib.attn_strerror.argtypes = [ctypes.c_int]
             lib.attn_strerror.restype = ctypes.c_char_p
             lib.attn_last_cuda_error.argtypes = []
@@ -218,6 +222,43 @@ def fwd_kv(q, k, v, mask: str = "none", scale: Optional[float] = None, out=None,
                      Nq, Nk, d, MASKS[mask], scale, _dtype_code(q), ws_ptr, ws_n, stream.cuda_stream,
                      checked=checked)
     _check(st, "attn_fwd_kv")
+    return out, lse
+
+
+def attn_fwd_kv_static(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, stream) -> int:
+    """Raw C call of attn_fwd_kv_static (integer pointers); returns the attn_status_t."""
+    return int(load().attn_fwd_kv_static(q, k, v, o, lse, B, H, Nq, Nk, d, int(mask), float(scale),
+                                         int(dtype), stream))
+
+
+def fwd_kv_static(q, k, v, out, lse, mask: str = "none", scale: Optional[float] = None,
+                  stream=None) -> Tuple[object, object]:
+    """:func:`fwd_kv` through attn_fwd_kv_static: nothing is allocated on this path, so
+    the caller passes ``out`` (like q) and ``lse`` (fp32 [B, H, Nq]). Calls on one device
+    share the library's static scratch and must not overlap in time."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] must agree on B, H and d")
+    if not (q.dtype == k.dtype == v.dtype == out.dtype):
+        raise TypeError("q, k, v and out must share one dtype")
+    if out.shape != q.shape or lse.shape != q.shape[:3] or lse.dtype != torch.float32:
+        raise ValueError("out must be like q and lse fp32 [B, H, Nq]")
+    for t in (q, k, v, out, lse):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, out and lse must be contiguous CUDA tensors")
+    if mask not in MASKS:
+        raise ValueError(f"mask must be one of {sorted(MASKS)}")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_fwd_kv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            B, H, Nq, Nk, d, MASKS[mask], scale, _dtype_code(q), stream.cuda_stream)
+    _check(st, "attn_fwd_kv_static")
     return out, lse
 
 

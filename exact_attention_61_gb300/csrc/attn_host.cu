@@ -62,6 +62,30 @@ uint32_t* status_ptr(int dev, cudaError_t* err) {
     return static_cast<uint32_t*>(p);
 }
 
+// Scratch of attn_fwd_kv_static: split partials live in this file-scope array instead
+// of caller memory. A plan needs B*H * splits * Nq * (d+1) * 4 bytes, and keys are split
+// only while B*H * ceil(Nq/256) < 304 with B*H * splits < 304 + B*H, so 8 MiB holds
+// every plan with Nq <= 16 (at most 607 * 16 * 129 * 4 bytes, about 5 MB).
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_kv_scratch[kStaticScratchBytes];
+
+// Device address of g_kv_scratch on the current device (looked up once per device).
+void* static_scratch_ptr(int dev, cudaError_t* err) {
+    static std::atomic<uintptr_t> cache[64];
+    if (dev >= 0 && dev < 64) {
+        uintptr_t v = cache[dev].load(std::memory_order_acquire);
+        if (v) return reinterpret_cast<void*>(v);
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_kv_scratch);
+    if (e != cudaSuccess) {
+        *err = e;
+        return nullptr;
+    }
+    if (dev >= 0 && dev < 64) cache[dev].store(reinterpret_cast<uintptr_t>(p), std::memory_order_release);
+    return p;
+}
+
 namespace {
 
 bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
@@ -311,6 +335,21 @@ int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, fl
     return checked(run_kv, &a, q, stream);
 }
 
+int attn_fwd_kv_static(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                       int64_t H, int64_t Nq, int64_t Nk, int64_t d, int mask, float scale, int dtype,
+                       void* stream) {
+    const int st = validate(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, nullptr, 0);
+    if (st != ATTN_OK) return st;
+    if (plan_split(B * H, Nq, Nk, d, SIZE_MAX).bytes > kStaticScratchBytes) return ATTN_ERR_SCRATCH_TOO_SMALL;
+    int dev = 0;
+    cudaError_t e = select_device_of(q, &dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* scratch = static_scratch_ptr(dev, &e);
+    if (!scratch) return cuda_fail(e);
+    return fwd_kv_impl(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, scratch, kStaticScratchBytes,
+                       stream);
+}
+
 const char* attn_strerror(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
@@ -319,6 +358,9 @@ const char* attn_strerror(int status) {
         case ATTN_ERR_MISALIGNED: return "misaligned pointer (all tensors must be 16-byte aligned)";
         case ATTN_ERR_CUDA: return "CUDA error (see attn_last_cuda_error)";
         case ATTN_ERR_TIMEOUT: return "device-side wait timed out (outputs undefined)";
+        case ATTN_ERR_SCRATCH_TOO_SMALL:
+            return "the split of the keys needs more than the 8 MiB static scratch of attn_fwd_kv_static "
+                   "(use attn_fwd_kv with a workspace)";
         default: return "unknown status";
     }
 }

@@ -69,8 +69,10 @@ typedef enum {
     ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned                        */
     ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed; see
                                   attn_last_cuda_error()                                  */
-    ATTN_ERR_TIMEOUT = 5       /* a device-side wait ran out (attn_fwd_checked only); the
+    ATTN_ERR_TIMEOUT = 5,      /* a device-side wait ran out (attn_fwd_checked only); the
                                   outputs are undefined and the context stays usable      */
+    ATTN_ERR_SCRATCH_TOO_SMALL = 6 /* attn_fwd_kv_static: the split of the keys for these
+                                  sizes needs more than its static scratch               */
 } attn_status_t;
 
 /*
@@ -148,6 +150,30 @@ int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, fl
  * its full split of the keys for these sizes (0: it never splits them). Pure
  * host arithmetic, no CUDA call; 0 for sizes attn_fwd_kv rejects. */
 size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d);
+
+/*
+ * attn_fwd_kv_static -- attn_fwd_kv that allocates nothing and takes no
+ * workspace: the split partials go to a static device array of 8 MiB
+ * (8388608 bytes) inside this library. The
+ * pages have no counterpart; it exists for callers that must not allocate or
+ * pass device scratch on the call path.
+ *  - Arguments, masks and results as attn_fwd_kv. Sizes whose full split of
+ *    the keys needs more than the scratch (attn_fwd_kv_workspace_bytes(...) >
+ *    8388608) are rejected with ATTN_ERR_SCRATCH_TOO_SMALL before anything is
+ *    enqueued. Every size with Nq <= 16 fits.
+ *  - Nothing in the scratch needs to start at zero: each call writes every
+ *    partial it reads before reading it.
+ *  - No device or host memory is allocated (no cudaMalloc/cudaFree, no
+ *    allocating library). The first call on a device looks up the scratch
+ *    address with cudaGetSymbolAddress (that device current) and caches it;
+ *    make that first call before any stream capture.
+ *  - There is one scratch per device: calls that may overlap in time (other
+ *    streams, other host threads) race on it and give wrong results.
+ *    Serialise them, or use attn_fwd_kv with a workspace of their own.
+ */
+int attn_fwd_kv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int mask,
+                       float scale, int dtype, void* stream);
 
 /* attn_strerror -- static, human-readable text for an attn_status_t. Never NULL. */
 const char* attn_strerror(int status);

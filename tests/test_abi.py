@@ -47,7 +47,7 @@ def test_library_targets_sm103a():
 
 def test_strerror(lib):
     from exact_attention_61_gb300 import attn
-    for st in range(6):
+    for st in range(7):
         assert attn.strerror(st)
     assert attn.strerror(99) == "unknown status"
 
@@ -154,3 +154,25 @@ def test_workspace_bytes_rejects_bad_sizes(lib):
     assert attn.workspace_bytes(0, 1, 1, 100, 64) == 0
     assert attn.workspace_bytes(1, 1, 1, 100, 96) == 0
     assert attn.workspace_bytes(1, 1, 1, 0, 64) == 0
+
+
+def test_static_scratch_entry_rejects_before_any_cuda_call(lib):
+    """attn_fwd_kv_static validates like attn_fwd_kv and refuses sizes whose split needs
+    more than its 8 MiB static scratch, all on the host (fake pointers here)."""
+    from exact_attention_61_gb300 import attn
+    args = dict(q=A, k=2 * A * 64, v=3 * A * 64, o=4 * A * 64, lse=5 * A * 64, B=1, H=2, Nq=4,
+                Nk=1000, d=64, mask=2, scale=0.125, dtype=1, stream=None)
+    assert attn.attn_fwd_kv_static(**{**args, "q": 0}) == 1
+    assert attn.attn_fwd_kv_static(**{**args, "mask": 7}) == 1
+    assert attn.attn_fwd_kv_static(**{**args, "d": 96}) == 2
+    assert attn.attn_fwd_kv_static(**{**args, "lse": 5 * A * 64 + 4}) == 3
+    big = dict(B=1, H=64, Nq=256, Nk=65536, d=128)
+    assert attn.workspace_bytes(**big) > attn.STATIC_SCRATCH_BYTES
+    G = 1 << 32  # fake addresses far enough apart for these sizes
+    spaced = dict(q=G, k=2 * G, v=3 * G, o=4 * G, lse=5 * G)
+    assert attn.attn_fwd_kv_static(**{**args, **big, **spaced}) == attn.ATTN_ERR_SCRATCH_TOO_SMALL
+    assert "static scratch" in attn.strerror(attn.ATTN_ERR_SCRATCH_TOO_SMALL)
+    # every size with at most 16 query rows fits
+    for BH in (1, 7, 100, 151, 152, 303):
+        for d in (64, 128):
+            assert attn.workspace_bytes(1, BH, 16, 1 << 20, d) <= attn.STATIC_SCRATCH_BYTES
