@@ -422,6 +422,94 @@ def run_ours(args) -> int:
     return 0
 
 
+def decode_bytes(B_: int, H_: int, Nq: int, Nk: int, d: int, elem: int = 2) -> int:
+    """Algorithmic HBM bytes of one decode step: Q, K and V read once, O and the fp32
+    LSE written once (the split partials are the implementation's own traffic)."""
+    return elem * B_ * H_ * d * (2 * Nq + 2 * Nk) + 4 * B_ * H_ * Nq
+
+
+def run_decode(args) -> int:
+    """--decode NAME: one KV-cache decode step per timed step (attn_fwd_kv, bottom-right
+    causal mask, split of the keys + merge), reported as HBM GB/s against the measured
+    copy bandwidth. Single GPU; an extra measurement beside the headline line."""
+    import torch
+
+    from exact_attention_61_gb300 import attn
+    from gen import decode_workload, make_qkv_kv
+
+    w = decode_workload(args.decode)
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    attn.load()
+    q, k, v = (t.to(dev) for t in make_qkv_kv(w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, w.seed))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    ws_n = attn.workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = 1.0 / math.sqrt(w.d)
+    dt = attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_FP16
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def launch():
+        st = attn.attn_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              w.B, w.H, w.Nq, w.Nk, w.d, attn.ATTN_MASK_CAUSAL_BOTTOM_RIGHT, scale, dt,
+                              ws.data_ptr(), ws_n, stream.cuda_stream)
+        if st != attn.ATTN_OK:
+            raise RuntimeError(f"attn_fwd_kv failed: {attn.strerror(st)}")
+
+    sampler = ClockSampler(0) if args.clocks else None
+    t_w = time.perf_counter()
+    n_warm = 0
+    while n_warm < args.warmup or time.perf_counter() - t_w < args.warmup_seconds:
+        flush.fill_(n_warm & 0xFF)
+        launch()
+        n_warm += 1
+        if n_warm % 16 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        launch()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if sampler:
+        sampler.stop()
+    t_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = statistics.fmean(t_ms)
+    nbytes = decode_bytes(w.B, w.H, w.Nq, w.Nk, w.d)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    splits = ws_n // (w.B * w.H * w.Nq * (w.d + 1) * 4) if ws_n else 1
+    out = {
+        "metric": f"decode attention HBM GB/s ({w.name})", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": n_warm, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "mask": "causal_bottom_right", "key_splits": splits, "seed": w.seed,
+                   "l2": "flushed before every step (write of 2x L2 size, outside the events)"},
+        "ms_median": statistics.median(t_ms), "ms_p10": _pct(t_ms, 10), "ms_p90": _pct(t_ms, 90),
+        "roofline": {"bound": "hbm", "kernel": "attn_fwd_kernel split + attn_merge_kernel (one call)",
+                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_step": nbytes,
+                     "peak_source": "measured copy (MEASURED_PEAKS.json)"
+                     if peaks["source"] == "measured" else "fallback 6.8 TB/s"},
+        "gpu_launches": (2 if ws_n else 1) * args.steps,
+    }
+    if sampler:
+        out["clocks"] = summarize_clocks(sampler.samples, t0 - args.warmup_seconds, t1)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def _pct(xs, p):
     s = sorted(xs)
     return s[min(len(s) - 1, max(0, int(round(p / 100.0 * (len(s) - 1)))))]
@@ -440,6 +528,8 @@ def parse_args(argv=None):
                     help="CPU work per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--decode", default=None, metavar="NAME",
+                    help="time a KV-cache decode workload instead (extra measurement, 1 GPU)")
     return ap.parse_args(argv)
 
 
@@ -449,6 +539,8 @@ def main(argv=None) -> int:
         raise SystemExit("--steps must be >= 1")
     if args.impl == "reference":
         return run_reference(args)
+    if args.decode:
+        return run_decode(args)
     return run_ours(args)
 
 

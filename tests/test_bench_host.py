@@ -107,3 +107,15 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"],
                    {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_decode_bytes():
+    import bench
+    # b8h32q1k8192d128 bf16: K and V dominate; Q, O and LSE add a little
+    kv = 2 * 8 * 32 * 8192 * 128 * 2
+    qo = 2 * 8 * 32 * 1 * 128 * 2
+    assert bench.decode_bytes(8, 32, 1, 8192, 128) == kv + qo + 4 * 8 * 32
+    from gen import DECODE_WORKLOADS, decode_workload
+    for w in DECODE_WORKLOADS:
+        assert decode_workload(w.name) is w
+    assert bench.parse_args(["--decode", "b8h32q1k8192d128"]).decode == "b8h32q1k8192d128"
