@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the exact scaled-dot-product attention forward.
+"""fp64 CPU oracle for the exact scaled-dot-product attention forward and backward.
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import this package; the CUDA path neither
@@ -19,6 +19,11 @@ Three functions compute the same thing three ways, so that each checks the other
   L = (m + log2 l) ln 2. An optional threshold ``tau`` keeps a stale maximum
   until the row maximum grows by more than ``tau`` (log2 units); the result is
   the same because O and l always share the maximum they were scaled by.
+
+The backward (the gradients of sum(dO * O)) has the same pair: :func:`attn_bwd`
+in C, the chain rule through the definition per query row, and
+:func:`attn_bwd_materialised` in numpy on whole matrices. The forward-only
+variants :func:`attn_fwd_qk` (Nq query rows against Nk keys) follow the forward.
 
 Inputs are 16-bit (or fp32/fp64) tensors/arrays of shape [B, H, N, d]; they are
 upcast exactly to fp64 before any arithmetic. Outputs are fp64: O [B, H, N, d]
@@ -77,6 +82,10 @@ def _load():
                                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                ctypes.c_int, ctypes.c_double]
             lib.oracle_attn_fwd_qk.restype = ctypes.c_int
+            lib.oracle_attn_bwd.argtypes = [_DP, _DP, _DP, _DP, _DP, _DP, _DP, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                            ctypes.c_double]
+            lib.oracle_attn_bwd.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -248,3 +257,51 @@ def attn_fwd_online(q, k, v, causal: bool, scale: float | None = None,
             o_out[b, h] = acc / l
             lse_out[b, h] = ((m + np.log2(l)) * math.log(2.0))[:, 0]
     return o_out, lse_out
+
+
+def attn_bwd(q, k, v, dout, causal: bool, scale: float | None = None):
+    """Gradients (dQ, dK, dV) of sum(dO * O) for O = attention(Q, K, V) (C, fp64).
+
+    The chain rule through the definition, per query row: P = exp(s - LSE),
+    dV += P^T dO, dP = dO V^T, D = rowsum(P * dP), dS = P * (dP - D),
+    dQ = scale dS K, dK = scale dS^T Q. All inputs [B,H,N,d]; returns three
+    float64 arrays of that shape.
+    """
+    q64, k64, v64, g64 = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    B, H, N, d = q64.shape
+    for t in (k64, v64, g64):
+        if t.shape != q64.shape:
+            raise ValueError("q, k, v and dout must have the same shape")
+    scale = default_scale(d) if scale is None else float(scale)
+    dq, dk, dv = (np.empty_like(q64) for _ in range(3))
+    rc = _load().oracle_attn_bwd(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B * H, N, d, int(bool(causal)), scale)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd failed with code {rc}")
+    return dq, dk, dv
+
+
+def attn_bwd_materialised(q, k, v, dout, causal: bool, scale: float | None = None):
+    """numpy fp64 twin of :func:`attn_bwd` on whole N x N matrices.
+
+    Returns a dict with dq, dk, dv and the intermediates p (softmax weights), dp
+    (dO V^T), ds (P * (dP - D)) and D, all float64.
+    """
+    q64, k64, v64, g64 = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    N, d = q64.shape[2], q64.shape[3]
+    scale = default_scale(d) if scale is None else float(scale)
+    s = scale * np.einsum("bhid,bhjd->bhij", q64, k64)
+    if causal:
+        s = np.where(np.tril(np.ones((N, N), dtype=bool)), s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    p = e / e.sum(axis=-1, keepdims=True)
+    dp = np.einsum("bhid,bhjd->bhij", g64, v64)
+    D = (p * dp).sum(axis=-1, keepdims=True)
+    ds = p * (dp - D)
+    return {
+        "dq": scale * np.einsum("bhij,bhjd->bhid", ds, k64),
+        "dk": scale * np.einsum("bhij,bhid->bhjd", ds, q64),
+        "dv": np.einsum("bhij,bhid->bhjd", p, g64),
+        "p": p, "dp": dp, "ds": ds, "D": D[..., 0],
+    }

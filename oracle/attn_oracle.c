@@ -213,6 +213,88 @@ int oracle_attn_fwd_qk(const double* q, const double* k, const double* v, double
     return failed ? -2 : 0;
 }
 
+/* Backward of the forward above: the vector-Jacobian product of O = attn(Q, K, V)
+ * with an upstream gradient dO, i.e. the gradients of sum(dO * O) with respect to
+ * Q, K and V. "如何用 profiler 逐步优化 Triton FlashAttention-2 kernel", "Future
+ * articles", names it as the FA2 backward that consumes the saved L; the forward
+ * there is a torch.autograd.Function, so its backward is the chain rule through the
+ * definition, written out per query row i over its visible keys j:
+ *
+ *   P_ij  = exp(s_ij - LSE_i)             softmax weights (LSE of the row itself)
+ *   dV_j += P_ij dO_i                     O_i = sum_j P_ij v_j
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_j P_ij dP_ij              (equals dO_i . O_i)
+ *   dS_ij = P_ij (dP_ij - D_i)            Jacobian of the row softmax
+ *   dQ_i  = scale sum_j dS_ij k_j         s_ij = scale q_i . k_j
+ *   dK_j += scale dS_ij q_i
+ *
+ * q, k, v, dout, dq, dk, dv: [BH][N][d]. One head per OpenMP task, rows in order,
+ * so the result does not depend on the thread count. */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv, int64_t BH, int64_t N, int64_t d,
+                    int causal, double scale)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || BH < 1 || N < 1 || d < 1) return -1;
+    if (!(scale > 0.0) || !isfinite(scale)) return -1;
+    int failed = 0;
+#pragma omp parallel reduction(| : failed)
+    {
+        double* p = (double*)malloc((size_t)N * sizeof(double));
+        double* dp = (double*)malloc((size_t)N * sizeof(double));
+        if (!p || !dp) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bh = 0; bh < BH; ++bh) {
+                const double* Q = q + bh * N * d;
+                const double* K = k + bh * N * d;
+                const double* V = v + bh * N * d;
+                const double* DO = dout + bh * N * d;
+                double* DQ = dq + bh * N * d;
+                double* DK = dk + bh * N * d;
+                double* DV = dv + bh * N * d;
+                memset(DK, 0, (size_t)(N * d) * sizeof(double));
+                memset(DV, 0, (size_t)(N * d) * sizeof(double));
+                for (int64_t i = 0; i < N; ++i) {
+                    const int64_t n_vis = causal ? i + 1 : N;
+                    const double* qi = Q + i * d;
+                    const double* doi = DO + i * d;
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < n_vis; ++j) {
+                        double dot = 0.0;
+                        for (int64_t t = 0; t < d; ++t) dot += qi[t] * K[j * d + t];
+                        p[j] = scale * dot;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double l = 0.0;
+                    for (int64_t j = 0; j < n_vis; ++j) l += exp(p[j] - m);
+                    const double lse = m + log(l);
+                    double Di = 0.0;
+                    for (int64_t j = 0; j < n_vis; ++j) {
+                        p[j] = exp(p[j] - lse);
+                        double dot = 0.0;
+                        for (int64_t t = 0; t < d; ++t) dot += doi[t] * V[j * d + t];
+                        dp[j] = dot;
+                        Di += p[j] * dot;
+                    }
+                    for (int64_t t = 0; t < d; ++t) DQ[i * d + t] = 0.0;
+                    for (int64_t j = 0; j < n_vis; ++j) {
+                        const double ds = p[j] * (dp[j] - Di);
+                        for (int64_t t = 0; t < d; ++t) {
+                            DV[j * d + t] += p[j] * doi[t];
+                            DQ[i * d + t] += scale * ds * K[j * d + t];
+                            DK[j * d + t] += scale * ds * qi[t];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return failed ? -2 : 0;
+}
+
 /* Threads an OpenMP parallel region of this library uses. */
 int oracle_num_threads(void)
 {
