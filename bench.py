@@ -510,6 +510,100 @@ def run_decode(args) -> int:
     return 0
 
 
+def bwd_flops(B_: int, H_: int, N_: int, d: int, causal: bool) -> float:
+    """Algorithmic FLOPs of the backward: five N x N x d products (S, dP, dV, dK, dQ)
+    against the forward's two, i.e. 2.5 x 4 B H N^2 d, halved under the causal mask."""
+    f = 10.0 * B_ * H_ * N_ * N_ * d
+    return f / 2 if causal else f
+
+
+def run_bwd(args) -> int:
+    """--bwd: one backward pass (prep + main kernel + dQ cast) per timed step on the
+    headline problem, non-causal then causal, reported as TFLOP/s against the
+    measured bf16 peak. Single GPU; an extra measurement beside the headline line."""
+    import torch
+
+    from exact_attention_61_gb300 import attn
+    from gen import make_qkv
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    attn.load()
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, N, D, DTYPE, SEED))
+    do = make_qkv(B, H, N, D, DTYPE, SEED + 7919)[0].to(dev)
+    scale = 1.0 / math.sqrt(D)
+    outs = {c: attn.fwd(q, k, v, causal=c, scale=scale, checked=True) for c in (False, True)}
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws_n = attn.bwd_workspace_bytes(B, H, N, D)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def launch(causal):
+        o, lse = outs[causal]
+        st = attn.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
+                           causal, scale, attn.ATTN_BF16, ws.data_ptr(), ws_n, stream.cuda_stream)
+        if st != attn.ATTN_OK:
+            raise RuntimeError(f"attn_bwd failed: {attn.strerror(st)}")
+
+    sampler = ClockSampler(0) if args.clocks else None
+    t_w = time.perf_counter()
+    n_warm = 0
+    while n_warm < args.warmup or time.perf_counter() - t_w < args.warmup_seconds:
+        flush.fill_(n_warm & 0xFF)
+        launch(False)
+        launch(True)
+        n_warm += 1
+        if n_warm % 16 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        launch(False)
+        ev[i][1].record(stream)
+        launch(True)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if sampler:
+        sampler.stop()
+    t_nc = [e[0].elapsed_time(e[1]) for e in ev]
+    t_c = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_nc, ms_c = statistics.fmean(t_nc), statistics.fmean(t_c)
+    f_nc, f_c = bwd_flops(B, H, N, D, False), bwd_flops(B, H, N, D, True)
+    peaks = measured_peaks()
+    ach = tflops(f_nc, ms_nc)
+    out = {
+        "metric": "attention bwd TFLOP/s at B=4,H=16,N=4096,d=64 bf16", "value": tflops(f_nc + f_c, ms_nc + ms_c),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": n_warm,
+        "ms_per_step": ms_nc + ms_c, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "b4h16n4096d64 bf16 backward, non-causal + causal per step", "B": B, "H": H,
+                   "N": N, "d": D, "scale": scale, "seed": SEED,
+                   "flops": "10 B H N^2 d (five N x N x d products), halved for causal",
+                   "l2": "flushed before every step (write of 2x L2 size, outside the events)"},
+        "per_kernel": {"noncausal": {"ms_mean": ms_nc, "ms_median": statistics.median(t_nc),
+                                     "tflops": tflops(f_nc, ms_nc)},
+                       "causal": {"ms_mean": ms_c, "ms_median": statistics.median(t_c),
+                                  "tflops": tflops(f_c, ms_c)}},
+        "roofline": {"bound": "tensor", "kernel": "attn_bwd (prep + attn_bwd_kernel + dQ cast), non-causal",
+                     "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                     "algorithmic_flops_per_launch": f_nc},
+        "gpu_launches": 6 * args.steps,
+    }
+    if sampler:
+        out["clocks"] = summarize_clocks(sampler.samples, t0 - args.warmup_seconds, t1)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def _pct(xs, p):
     s = sorted(xs)
     return s[min(len(s) - 1, max(0, int(round(p / 100.0 * (len(s) - 1)))))]
@@ -528,6 +622,8 @@ def parse_args(argv=None):
                     help="CPU work per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward pass instead (extra measurement, 1 GPU)")
     ap.add_argument("--decode", default=None, metavar="NAME",
                     help="time a KV-cache decode workload instead (extra measurement, 1 GPU)")
     return ap.parse_args(argv)
@@ -541,6 +637,8 @@ def main(argv=None) -> int:
         return run_reference(args)
     if args.decode:
         return run_decode(args)
+    if args.bwd:
+        return run_bwd(args)
     return run_ours(args)
 
 

@@ -47,6 +47,11 @@ _FWD_KV_ARGS = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void
                 ctypes.c_void_p]
 
 
+_BWD_ARGS = ([ctypes.c_void_p] * 9 + [ctypes.c_int64] * 4 +
+             [ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+              ctypes.c_void_p])
+
+
 class AttnError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(msg)
@@ -75,6 +80,12 @@ def load(path: str = LIB_PATH):
             lib.attn_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_fwd_kv_static.argtypes = _FWD_KV_ARGS[:13] + [ctypes.c_void_p]
             lib.attn_fwd_kv_static.restype = ctypes.c_int
+            lib.attn_bwd.argtypes = _BWD_ARGS
+            lib.attn_bwd.restype = ctypes.c_int
+            lib.attn_bwd_checked.argtypes = _BWD_ARGS
+            lib.attn_bwd_checked.restype = ctypes.c_int
+            lib.attn_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 4
+            lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_strerror.argtypes = [ctypes.c_int]
             lib.attn_strerror.restype = ctypes.c_char_p
             lib.attn_last_cuda_error.argtypes = []
@@ -223,6 +234,57 @@ def fwd_kv(q, k, v, mask: str = "none", scale: Optional[float] = None, out=None,
                      checked=checked)
     _check(st, "attn_fwd_kv")
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, dtype, workspace,
+             workspace_bytes, stream, checked: bool = False) -> int:
+    """Raw C call of attn_bwd (or attn_bwd_checked); returns the attn_status_t."""
+    lib = load()
+    fn = lib.attn_bwd_checked if checked else lib.attn_bwd
+    return int(fn(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, int(bool(causal)), float(scale),
+                  int(dtype), workspace, int(workspace_bytes), stream))
+
+
+def bwd_workspace_bytes(B, H, N, d) -> int:
+    """Workspace attn_bwd needs for these sizes (0 for sizes it rejects)."""
+    return int(load().attn_bwd_workspace_bytes(B, H, N, d))
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, dq=None,
+        dk=None, dv=None, workspace=None, stream=None, checked: bool = False):
+    """Gradients (dq, dk, dv) of sum(dout * o) for o, lse = fwd(q, k, v, causal, scale).
+
+    All tensors contiguous CUDA [B, H, N, d] of one 16-bit dtype; lse fp32 [B, H, N].
+    ``workspace`` (a CUDA uint8 tensor of :func:`bwd_workspace_bytes` bytes) is
+    allocated here when not given.
+    """
+    import torch
+    for t in (q, k, v, o, dout):
+        if t.dim() != 4 or t.shape != q.shape:
+            raise ValueError("q, k, v, o and dout must all be [B, H, N, d]")
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v, o and dout must share one dtype")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty((max(bwd_workspace_bytes(B, H, N, d), 16),), dtype=torch.uint8,
+                                device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                  dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, causal,
+                  scale, _dtype_code(q), workspace.data_ptr(), workspace.numel(), stream.cuda_stream,
+                  checked=checked)
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_kv_static(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, stream) -> int:

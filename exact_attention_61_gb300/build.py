@@ -6,6 +6,8 @@ with the CUDA runtime linked statically):
   probe.cu                           one-tile tensor-core probe (test hook)
   attn_merge.cu                      merge of split-key partials
   attn_fwd_inst.cu x 4               forward kernel, one unit per (d, dtype)
+  attn_bwd_aux.cu                    backward prologue (D, lse2) and dQ cast
+  attn_bwd_inst.cu x 4               backward kernel, one unit per (d, dtype)
 """
 from __future__ import annotations
 
@@ -34,6 +36,11 @@ UNITS = [
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=1"], "attn_fwd_d64_bf16.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=128", "-DATTN_INST_BF16=0"], "attn_fwd_d128_f16.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=128", "-DATTN_INST_BF16=1"], "attn_fwd_d128_bf16.o"),
+    ("attn_bwd_aux.cu", [], "attn_bwd_aux.o"),
+    ("attn_bwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=0"], "attn_bwd_d64_f16.o"),
+    ("attn_bwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=1"], "attn_bwd_d64_bf16.o"),
+    ("attn_bwd_inst.cu", ["-DATTN_INST_D=128", "-DATTN_INST_BF16=0"], "attn_bwd_d128_f16.o"),
+    ("attn_bwd_inst.cu", ["-DATTN_INST_D=128", "-DATTN_INST_BF16=1"], "attn_bwd_d128_bf16.o"),
 ]
 
 

@@ -1,0 +1,52 @@
+// One (head dimension, dtype) pair of backward-kernel instances, causal or not.
+// Compiled once per pair with -DATTN_INST_D=<64|128> -DATTN_INST_BF16=<0|1>.
+#include <atomic>
+
+#include "attn_bwd_internal.h"
+#include "attn_bwd_kernel.cuh"
+
+#if !defined(ATTN_INST_D) || !defined(ATTN_INST_BF16)
+#error "compile with -DATTN_INST_D=<64|128> -DATTN_INST_BF16=<0|1>"
+#endif
+
+namespace attn_sm103 {
+namespace {
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_bwd_one(const CUtensorMap* m, const BwdParams& p, cudaStream_t s) {
+    using C = BwdCfg<D>;
+    auto* kern = attn_bwd_kernel<D, CAUSAL, BF16>;
+    // The dynamic shared-memory opt-in is per device; remember which devices have it.
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const unsigned grid = static_cast<unsigned>(p.n_tiles) * static_cast<unsigned>(p.BH);
+    kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+#define ATTN_CAT2(a, b) a##b
+#define ATTN_CAT(a, b) ATTN_CAT2(a, b)
+#if ATTN_INST_BF16
+#define ATTN_DT_SUFFIX bf16
+#else
+#define ATTN_DT_SUFFIX f16
+#endif
+#define ATTN_BWD_NAME ATTN_CAT(ATTN_CAT(ATTN_CAT(launch_bwd_d, ATTN_INST_D), _), ATTN_DT_SUFFIX)
+
+cudaError_t ATTN_BWD_NAME(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
+    constexpr bool kBf16 = ATTN_INST_BF16 != 0;
+    return causal ? launch_bwd_one<ATTN_INST_D, true, kBf16>(maps, p, s)
+                  : launch_bwd_one<ATTN_INST_D, false, kBf16>(maps, p, s);
+}
+
+}  // namespace attn_sm103

@@ -1,0 +1,480 @@
+// Exact attention backward for sm_103a: dQ, dK, dV of sum(dO * O) from the saved LSE.
+//
+// What it computes, per head, for keys j and query rows i that see them
+// (natural-log LSE from the forward, D_i = dO_i . O_i):
+//   P_ij  = exp(scale q_i.k_j - LSE_i)
+//   dV_j  = sum_i P_ij dO_i
+//   dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i)
+//   dK_j  = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
+// This is the FlashAttention-2 backward that "如何用 profiler 逐步优化 Triton
+// FlashAttention-2 kernel" ("Future articles") names as the next kernel: it
+// consumes the L the forward writes ("Round 4 / exp2": natural-log units), and
+// it has two accumulations in different directions (dK, dV over query rows; dQ
+// over key tiles).
+//
+// GB300 design:
+//  - one CTA owns one 128-key tile of one head and loops over the 128-row Q tiles
+//    that see it (all of them, or those from the diagonal on under the causal
+//    mask). K and V stay in shared memory; Q, dO and the per-row LSE/D vectors
+//    stream through a TMA ring;
+//  - one warp issues the tcgen05 MMAs, all into tensor memory:
+//      S^T  = K Q^T     (128 keys x 128 queries, fp32)
+//      dP^T = V dO^T    (128 x 128, fp32)
+//      dV  += P^T dO    (P^T 16-bit in TMEM over S^T; dO MN-major in SMEM)
+//      dK  += dS^T Q    (dS^T 16-bit in TMEM over dP^T; Q MN-major in SMEM)
+//      dQ   = dS K      (dS 16-bit in SMEM, MN-major; K MN-major in SMEM)
+//  - one warpgroup, one thread per key row (= TMEM lane), turns S^T and dP^T
+//    into P^T and dS^T with exp2 and the LSE folded in log2 units, writes dS
+//    for the dQ product to shared memory, then adds the dQ tile into an fp32
+//    workspace with vector atomics (dQ gathers over key tiles owned by other
+//    CTAs);
+//  - dK and dV stay in TMEM for the whole loop and are stored once at the end;
+//  - every mbarrier wait is bounded, as in the forward kernel.
+#pragma once
+
+#include "attn_bwd_internal.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace attn_sm103 {
+
+enum : uint32_t { kRoleBwdLoad = 5, kRoleBwdMma = 6, kRoleBwdCompute = 7 };
+constexpr uint32_t kErrSmemAlign = 2u;
+
+// ---- tcgen05 / bulk-copy forms only the backward uses ------------------------------------
+
+// D = A B over 128 rows of K with both operands MN-major in shared memory: 8 MMAs of
+// K = 16, each advancing 16 rows = 2048 bytes = 128 descriptor units on A and on B.
+__device__ __forceinline__ void mma_mn128_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, one;\n\t.reg .b64 ad, bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 one, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.u64 ad, %1, 128;\n\tadd.u64 bd, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 256;\n\tadd.u64 bd, %2, 256;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 384;\n\tadd.u64 bd, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 512;\n\tadd.u64 bd, %2, 512;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 640;\n\tadd.u64 bd, %2, 640;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 768;\n\tadd.u64 bd, %2, 768;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t"
+        "add.u64 ad, %1, 896;\n\tadd.u64 bd, %2, 896;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, one;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor with the major-ness of A chosen too (bit 15; A from SMEM).
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc_ab(bool bf16, int M, int N, bool a_mn_major,
+                                                           bool b_mn_major) {
+    return idesc_f16_f32acc(bf16, M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
+// Warp-wide: thread t writes 16 consecutive 32-bit columns of TMEM lane (lane_base + t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// Global -> shared plain bulk copy of `bytes` (multiple of 16; both addresses 16-byte
+// aligned); completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// ---- configuration -----------------------------------------------------------------------
+
+template <int D>
+struct BwdCfg {
+    static_assert(D == 64 || D == 128, "head dimension must be 64 or 128");
+    static constexpr int kStages = D == 64 ? 3 : 2;    // Q/dO ring depth
+    static constexpr int kBoxBytes = 128 * 128;         // one TMA box: 128 rows x 64 elements x 2 B
+    static constexpr int kChunks = D / 64;              // boxes per 128-row tile
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffDS = kOffV + kTileBytes;   // dS: 128 keys x 128 queries, MN-major
+    static constexpr int kOffStage = kOffDS + 128 * 128 * 2;
+    static constexpr int kStageBytes = 2 * kTileBytes;  // Q, then dO
+    static constexpr int kOffVec = kOffStage + kStages * kStageBytes;
+    static constexpr int kVecBytes = 2 * 128 * 4;       // lse2[128], D[128] per stage
+    static constexpr int kOffBar = kOffVec + kStages * kVecBytes;
+    static constexpr int kBarKV = 0;
+    static constexpr int kBarQdFull = 1;
+    static constexpr int kBarQdEmpty = kBarQdFull + kStages;
+    static constexpr int kBarSdp = kBarQdEmpty + kStages;  // S^T and dP^T in TMEM
+    static constexpr int kBarPds = kBarSdp + 1;            // P^T, dS^T in TMEM and dS in SMEM
+    static constexpr int kBarDqFull = kBarPds + 1;         // dQ tile in TMEM
+    static constexpr int kBarDqRead = kBarDqFull + 1;      // dQ tile read out
+    static constexpr int kBarAcc = kBarDqRead + 1;         // dK, dV final
+    static constexpr int kBarDrain = kBarAcc + 1;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    // The dynamic shared-memory base is 1024-byte aligned (declared so and checked at
+    // run time): d = 128 leaves no room for alignment slack.
+    static constexpr int kSmemBytes = kOffMisc + 16;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    // TMEM columns: S^T/P^T, dP^T/dS^T, dV, dK, and the dQ tile (d = 128: over S^T).
+    static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
+    static constexpr uint32_t colDQ = D == 64 ? 384u : 0u;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kThreads = 192;  // warps 0-3 compute, 4 MMA, 5 TMA
+    static constexpr int kWarpMma = 4;
+    static constexpr int kWarpLoad = 5;
+};
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_bwd[];
+    const uint32_t base = smem_addr(smem_bwd);
+    if (base & 1023u) {  // uniform over the CTA: nothing has been set up yet
+        if (threadIdx.x == 0) {
+            if (atomicCAS(p.err, 0u, kErrSmemAlign) == 0u) p.err[1] = blockIdx.x;
+        }
+        return;
+    }
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31u;
+    auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * i; };
+    auto sQ = [&](int s) -> uint32_t { return base + C::kOffStage + s * C::kStageBytes; };
+    auto sDO = [&](int s) -> uint32_t { return sQ(s) + C::kTileBytes; };
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem_bwd + C::kOffMisc);  // [0] tmem, [1] abort
+
+    // Heaviest key tiles first: under the causal mask key tile 0 sees every Q tile.
+    const int bh = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.BH));
+    const int kt = static_cast<int>(blockIdx.x / static_cast<uint32_t>(p.BH));
+    const int N = p.N;
+    const int j0 = kt * 128;
+    const int qt0 = CAUSAL ? kt : 0;
+    const int n_it = p.n_tiles - qt0;  // >= 1
+    WaitCtx wc{p.err, misc + 1, blockIdx.x};
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages) count = 1 + 4;  // MMA + 4 warps
+            if (i == C::kBarPds || i == C::kBarDqRead) count = 4;                        // one per warp
+            mbar_init(bar(i), count);
+        }
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == C::kWarpMma) {
+        tmem_alloc(smem_addr(misc), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    if (warp == C::kWarpLoad) {
+        // ================================ TMA producer ================================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            tma_prefetch_desc(&tmDO);
+            const uint64_t pol_kv = l2_policy_evict_first();  // read by this CTA only
+            const uint64_t pol_q = l2_policy_evict_last();    // read by every key tile of the head
+            mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d_hint(base + C::kOffK + c * C::kBoxBytes, &tmK, bar(C::kBarKV), c * 64, j0, bh, pol_kv);
+                tma_load_3d_hint(base + C::kOffV + c * C::kBoxBytes, &tmV, bar(C::kBarKV), c * 64, j0, bh, pol_kv);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % C::kStages;
+                if (it >= C::kStages &&
+                    !wait_one(bar(C::kBarQdEmpty + s), ((it / C::kStages) - 1) & 1, wc,
+                              kRoleBwdLoad * 1000 + C::kBarQdEmpty + s, it))
+                    break;
+                const int q0 = (qt0 + it) * 128;
+                const uint32_t fb = bar(C::kBarQdFull + s);
+                mbar_arrive_expect_tx(fb, 2 * C::kTileBytes + C::kVecBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d_hint(sQ(s) + c * C::kBoxBytes, &tmQ, fb, c * 64, q0, bh, pol_q);
+                    tma_load_3d_hint(sDO(s) + c * C::kBoxBytes, &tmDO, fb, c * 64, q0, bh, pol_q);
+                }
+                const size_t vrow = static_cast<size_t>(bh) * p.Npad + q0;
+                const uint32_t vdst = base + C::kOffVec + s * C::kVecBytes;
+                bulk_load(vdst, p.lse2 + vrow, 512, fb);
+                bulk_load(vdst + 512, p.dvec + vrow, 512, fb);
+                issued = it + 1;
+            }
+            // Drain: every copy into this CTA's shared memory has landed before it exits.
+            wait_one(bar(C::kBarKV), 0, wc, kRoleBwdLoad * 1000 + 90, 0, false);
+            for (int jj = max(0, issued - C::kStages); jj < issued; ++jj)
+                wait_one(bar(C::kBarQdFull + jj % C::kStages), (jj / C::kStages) & 1, wc,
+                         kRoleBwdLoad * 1000 + 91, jj, false);
+        }
+        __syncwarp();
+    } else if (warp == C::kWarpMma) {
+        // ================================ MMA issuer ==================================
+        constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, 128, 128, false);        // K-major x K-major
+        constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, 128, D, true);           // TMEM x MN-major
+        constexpr uint32_t idesc_q = idesc_f16_f32acc_ab(BF16, 128, D, true, true);  // MN x MN
+        const uint64_t dK_k = sdesc_sw128(base + C::kOffK, 16, 1024);            // K as A, K-major
+        const uint64_t dV_k = sdesc_sw128(base + C::kOffV, 16, 1024);            // V as A, K-major
+        const uint64_t dK_mn = sdesc_sw128(base + C::kOffK, C::kBoxBytes, 1024); // K as B, MN-major
+        const uint64_t dDS = sdesc_sw128(base + C::kOffDS, C::kBoxBytes, 1024);  // dS as A, MN-major
+        constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+        constexpr uint64_t kTileStep = C::kTileBytes >> 4;
+        const uint64_t dQ_k0 = sdesc_sw128(sQ(0), 16, 1024);
+        const uint64_t dQ_mn0 = sdesc_sw128(sQ(0), C::kBoxBytes, 1024);
+
+        bool ok = wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdMma * 1000 + C::kBarKV, 0);
+        for (int it = 0; it < n_it && ok; ++it) {
+            const int s = it % C::kStages;
+            if (!wait_warp(bar(C::kBarQdFull + s), (it / C::kStages) & 1, wc,
+                           kRoleBwdMma * 1000 + C::kBarQdFull + s, it)) {
+                ok = false;
+                break;
+            }
+            // d = 128: the dQ tile of the previous iteration lives in the S^T columns.
+            if (D == 128 && it > 0 &&
+                !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint64_t q_k = dQ_k0 + s * kStageStep;
+            const uint64_t do_k = q_k + kTileStep;
+            const uint64_t q_mn = dQ_mn0 + s * kStageStep;
+            const uint64_t do_mn = q_mn + kTileStep;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+                const uint64_t off = (c * C::kBoxBytes) >> 4;
+                mma_qk64_warp(tmem + C::colS, dK_k + off, q_k + off, idesc_s, c > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+                const uint64_t off = (c * C::kBoxBytes) >> 4;
+                mma_qk64_warp(tmem + C::colDP, dV_k + off, do_k + off, idesc_s, c > 0 ? 1u : 0u);
+            }
+            mma_commit_warp(bar(C::kBarSdp));
+            if (!wait_warp(bar(C::kBarPds), it & 1, wc, kRoleBwdMma * 1000 + C::kBarPds, it)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            mma_pv128_warp(tmem + C::colDV, tmem + C::colS, do_mn, idesc_o, it > 0 ? 1u : 0u);
+            mma_pv128_warp(tmem + C::colDK, tmem + C::colDP, q_mn, idesc_o, it > 0 ? 1u : 0u);
+            // d = 64: the dQ columns of the previous iteration must have been read out.
+            if (D == 64 && it > 0 &&
+                !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            mma_mn128_warp(tmem + C::colDQ, dDS, dK_mn, idesc_q, 0u);
+            mma_commit_warp(bar(C::kBarDqFull));
+            mma_commit_warp(bar(C::kBarQdEmpty + s));
+        }
+        if (ok) mma_commit_warp(bar(C::kBarAcc));
+        // Drain: all MMAs issued by this warp are complete before TMEM is freed.
+        mma_commit_warp(bar(C::kBarDrain));
+        wait_warp(bar(C::kBarDrain), 0, wc, kRoleBwdMma * 1000 + C::kBarDrain, 0, false);
+        __syncwarp();
+    } else {
+        // ================================ compute warpgroup ===========================
+        const uint32_t wq = warp;                    // TMEM lane quarter
+        const uint32_t r = wq * 32u + lane;          // key row in the tile = TMEM lane
+        const int j = j0 + static_cast<int>(r);      // this thread's key
+        const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
+        const float qk = p.qk_scale;
+        const uint32_t sDS = base + C::kOffDS;
+        bool ok = true;
+        for (int it = 0; it < n_it && ok; ++it) {
+            const int s = it % C::kStages;
+            const int q0 = (qt0 + it) * 128;
+            if (!wait_warp(bar(C::kBarQdFull + s), (it / C::kStages) & 1, wc,
+                           kRoleBwdCompute * 1000 + C::kBarQdFull + s, it) ||
+                !wait_warp(bar(C::kBarSdp), it & 1, wc, kRoleBwdCompute * 1000 + C::kBarSdp, it)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const float* vec = reinterpret_cast<const float*>(smem_bwd + C::kOffVec + s * C::kVecBytes);
+            const float* lse2 = vec;
+            const float* dvec = vec + 128;
+            const bool diag = CAUSAL && q0 == j0;  // only this Q tile has keys after queries
+            const bool key_out = j >= N;           // padded key row: P = 0
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(lane_base + C::colS + 32 * c, sr);
+                tmem_ld32(lane_base + C::colDP + 32 * c, dr);
+                tmem_ld_wait();
+                reg_fence(sr);
+                reg_fence(dr);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int col = 32 * c + e;
+                    float p0 = ex2_ftz(fmaf(__uint_as_float(sr[e]), qk, -lse2[col]));
+                    float p1 = ex2_ftz(fmaf(__uint_as_float(sr[e + 1]), qk, -lse2[col + 1]));
+                    if (key_out || (diag && static_cast<int>(r) > col)) p0 = 0.f;
+                    if (key_out || (diag && static_cast<int>(r) > col + 1)) p1 = 0.f;
+                    const float ds0 = p0 * (__uint_as_float(dr[e]) - dvec[col]);
+                    const float ds1 = p1 * (__uint_as_float(dr[e + 1]) - dvec[col + 1]);
+                    pk[e >> 1] = pack2<BF16>(p0, p1);
+                    dk[e >> 1] = pack2<BF16>(ds0, ds1);
+                }
+                tmem_st16(lane_base + C::colS + 16 * c, pk);
+                tmem_st16(lane_base + C::colDP + 16 * c, dk);
+                // dS for the dQ product: element (query m, key r) of an MN-major operand,
+                // 128-byte swizzle; queries 32c..32c+31 are 4 chunks of 8 in row r.
+                const uint32_t blk = sDS + (c >> 1) * C::kBoxBytes + r * 128u;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t chunk = (c & 1) * 4u + t;
+                    st_shared_v4(blk + ((chunk ^ (r & 7u)) << 4), dk[4 * t], dk[4 * t + 1], dk[4 * t + 2],
+                                 dk[4 * t + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(C::kBarPds));
+                mbar_arrive(bar(C::kBarQdEmpty + s));
+            }
+            // dQ tile: TMEM lane r is query q0 + r.
+            if (!wait_warp(bar(C::kBarDqFull), it & 1, wc, kRoleBwdCompute * 1000 + C::kBarDqFull, it)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const int qrow = q0 + static_cast<int>(r);
+            float* dst = p.dq_acc + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + C::colDQ + 32 * c, o);
+                tmem_ld_wait();
+                reg_fence(o);
+                if (qrow < N) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + e),
+                                  make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                              __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarDqRead));
+        }
+        // ---- epilogue: dV and dK rows of this thread's key ----------------------------
+        if (ok) ok = wait_warp(bar(C::kBarAcc), 0, wc, kRoleBwdCompute * 1000 + C::kBarAcc, n_it);
+        if (ok) {
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? C::colDV : C::colDK;
+                const float mul = which == 0 ? 1.f : p.scale;
+                uint8_t* out = static_cast<uint8_t*>(which == 0 ? p.dv : p.dk);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + col + 32 * c, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+                    if (j < N) {
+                        uint4* row = reinterpret_cast<uint4*>(out + ((static_cast<size_t>(bh) * N + j) * D + 32 * c) * 2);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+                            row[e >> 3] = make_uint4(
+                                pack2<BF16>(__uint_as_float(o[e]) * mul, __uint_as_float(o[e + 1]) * mul),
+                                pack2<BF16>(__uint_as_float(o[e + 2]) * mul, __uint_as_float(o[e + 3]) * mul),
+                                pack2<BF16>(__uint_as_float(o[e + 4]) * mul, __uint_as_float(o[e + 5]) * mul),
+                                pack2<BF16>(__uint_as_float(o[e + 6]) * mul, __uint_as_float(o[e + 7]) * mul));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == C::kWarpMma) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// D_i = rowsum(dO * O), lse2_i = LSE_i log2(e) (+inf where LSE = -inf or i >= N, so that
+// P = 0 there), and the zeroed dQ accumulator. One warp per row of [BH][Npad].
+template <bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams p) {
+    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = static_cast<int>(threadIdx.x & 31u);
+    if (row >= static_cast<long long>(p.BH) * p.Npad) return;
+    const int bh = static_cast<int>(row / p.Npad), i = static_cast<int>(row % p.Npad);
+    const size_t vrow = static_cast<size_t>(bh) * p.Npad + i;
+    if (i >= p.N) {
+        if (lane == 0) {
+            p.lse2[vrow] = INFINITY;
+            p.dvec[vrow] = 0.f;
+        }
+        return;
+    }
+    const size_t off = (static_cast<size_t>(bh) * p.N + i) * p.d;
+    const int per = p.d / 32;  // 2 or 4 elements per lane
+    float acc = 0.f;
+    for (int e = 0; e < per; ++e) {
+        float o, g;
+        if constexpr (BF16) {
+            o = __bfloat162float(static_cast<const __nv_bfloat16*>(p.o)[off + lane * per + e]);
+            g = __bfloat162float(static_cast<const __nv_bfloat16*>(p.dout)[off + lane * per + e]);
+        } else {
+            o = __half2float(static_cast<const __half*>(p.o)[off + lane * per + e]);
+            g = __half2float(static_cast<const __half*>(p.dout)[off + lane * per + e]);
+        }
+        acc = fmaf(o, g, acc);
+        p.dq_acc[off + lane * per + e] = 0.f;
+    }
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (lane == 0) {
+        const float l = p.lse[static_cast<size_t>(bh) * p.N + i];
+        p.lse2[vrow] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+        p.dvec[vrow] = acc;
+    }
+}
+
+// dQ = scale * dq_acc, rounded once to the dtype. Four elements per thread.
+template <bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_convert_kernel(const BwdConvertParams p) {
+    const long long i4 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+    if (i4 >= p.n) return;
+    const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + i4);
+    uint2 out = make_uint2(pack2<BF16>(a.x * p.scale, a.y * p.scale), pack2<BF16>(a.z * p.scale, a.w * p.scale));
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.dq) + i4 * 2) = out;
+}
+
+}  // namespace attn_sm103

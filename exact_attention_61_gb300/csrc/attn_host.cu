@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include "attn.h"
+#include "attn_bwd_internal.h"
 #include "attn_internal.h"
 
 namespace attn_sm103 {
@@ -291,6 +292,136 @@ int run_kv(void* ctx) {
                        a->dtype, a->ws, a->ws_bytes, a->stream);
 }
 
+// ---- backward ------------------------------------------------------------------------------
+
+struct BwdLayout {
+    int64_t Npad;
+    uint64_t lse2_off, dvec_off, dq_off, bytes;
+};
+
+BwdLayout bwd_layout(int64_t BH, int64_t N, int64_t d) {
+    BwdLayout L;
+    L.Npad = (N + kBwdTile - 1) / kBwdTile * kBwdTile;
+    L.lse2_off = 0;
+    L.dvec_off = static_cast<uint64_t>(BH) * L.Npad * 4u;
+    L.dq_off = 2 * L.dvec_off;
+    L.bytes = L.dq_off + static_cast<uint64_t>(BH) * N * d * 4u;
+    return L;
+}
+
+struct BwdArgs {
+    const void *q, *k, *v, *o;
+    const float* lse;
+    const void* dout;
+    void *dq, *dk, *dv;
+    int64_t B, H, N, d;
+    int causal;
+    float scale;
+    int dtype;
+    void* ws;
+    size_t ws_bytes;
+    void* stream;
+};
+
+int bwd_validate(const BwdArgs& a) {
+    if (!a.q || !a.k || !a.v || !a.o || !a.lse || !a.dout || !a.dq || !a.dk || !a.dv || !a.ws)
+        return ATTN_ERR_INVALID_ARG;
+    if (a.B < 1 || a.H < 1 || a.N < 1 || a.d < 1) return ATTN_ERR_INVALID_ARG;
+    if (a.dtype != ATTN_FP16 && a.dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (a.d != 64 && a.d != 128) return ATTN_ERR_UNSUPPORTED;
+    const void* ptrs[10] = {a.q, a.k, a.v, a.o, a.lse, a.dout, a.dq, a.dk, a.dv, a.ws};
+    for (const void* p : ptrs)
+        if (reinterpret_cast<uintptr_t>(p) % 16u) return ATTN_ERR_MISALIGNED;
+    const int64_t lim31 = (int64_t(1) << 31) - 1;
+    if (a.B > lim31 || a.H > lim31 || a.N > lim31 || a.B * a.H > lim31) return ATTN_ERR_UNSUPPORTED;
+    const int64_t BH = a.B * a.H;
+    if (BH > (int64_t(1) << 60) / (a.N * a.d)) return ATTN_ERR_UNSUPPORTED;
+    const BwdLayout L = bwd_layout(BH, a.N, a.d);
+    if ((L.Npad / kBwdTile) * BH > lim31) return ATTN_ERR_UNSUPPORTED;
+    if (a.ws_bytes < L.bytes) return ATTN_ERR_INVALID_ARG;
+    const uint64_t t = static_cast<uint64_t>(BH * a.N * a.d) * 2u;
+    const uint64_t lb = static_cast<uint64_t>(BH * a.N) * 4u;
+    // outputs (dq, dk, dv, workspace) overlap nothing
+    const void* outs[4] = {a.dq, a.dk, a.dv, a.ws};
+    const uint64_t osz[4] = {t, t, t, L.bytes};
+    const void* all[10] = {a.q, a.k, a.v, a.o, a.lse, a.dout, a.dq, a.dk, a.dv, a.ws};
+    const uint64_t asz[10] = {t, t, t, t, lb, t, t, t, t, L.bytes};
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 10; ++j)
+            if (all[j] != outs[i] && ranges_overlap(outs[i], osz[i], all[j], asz[j])) return ATTN_ERR_INVALID_ARG;
+    // an output given twice (dq == dk, say) is an overlap as well
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (outs[i] == outs[j]) return ATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 6; ++j)
+            if (outs[i] == all[j]) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+int bwd_impl(const BwdArgs& a) {
+    const int st = bwd_validate(a);
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    cudaError_t e = select_device_of(a.q, &dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaSuccess;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn(&e);
+    if (!enc) return cuda_fail(e);
+    uint32_t* status = status_ptr(dev, &e);
+    if (!status) return cuda_fail(e);
+    const int64_t BH = a.B * a.H;
+    const BwdLayout L = bwd_layout(BH, a.N, a.d);
+    alignas(64) CUtensorMap maps[4];
+    const void* ptrs[4] = {a.q, a.k, a.v, a.dout};
+    for (int i = 0; i < 4; ++i) {
+        const CUresult r = make_map(enc, &maps[i], ptrs[i], BH, a.N, a.d, a.dtype);
+        if (r != CUDA_SUCCESS) {
+            g_last_cuda_error = 100000 + static_cast<int>(r);
+            return ATTN_ERR_CUDA;
+        }
+    }
+    char* ws = static_cast<char*>(a.ws);
+    float* lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
+    float* dvec = reinterpret_cast<float*>(ws + L.dvec_off);
+    float* dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
+    const bool bf16 = a.dtype == ATTN_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+
+    BwdPrepParams pp{a.o, a.dout, a.lse, lse2, dvec, dq_acc, static_cast<int>(a.N), static_cast<int>(L.Npad),
+                     static_cast<int>(BH), static_cast<int>(a.d)};
+    e = launch_bwd_prep(bf16, pp, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    BwdParams p;
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    p.dq_acc = dq_acc;
+    p.dk = a.dk;
+    p.dv = a.dv;
+    p.err = status;
+    p.N = static_cast<int>(a.N);
+    p.Npad = static_cast<int>(L.Npad);
+    p.BH = static_cast<int>(BH);
+    p.n_tiles = static_cast<int>(L.Npad / kBwdTile);
+    p.qk_scale = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+    p.scale = a.scale;
+    const bool c = a.causal != 0;
+    if (a.d == 64)
+        e = bf16 ? launch_bwd_d64_bf16(c, maps, p, s) : launch_bwd_d64_f16(c, maps, p, s);
+    else
+        e = bf16 ? launch_bwd_d128_bf16(c, maps, p, s) : launch_bwd_d128_f16(c, maps, p, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    BwdConvertParams cp{dq_acc, a.dq, a.scale, static_cast<long long>(BH * a.N * a.d)};
+    e = launch_bwd_convert(bf16, cp, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+int run_bwd(void* ctx) { return bwd_impl(*static_cast<const BwdArgs*>(ctx)); }
+
 }  // namespace
 }  // namespace attn_sm103
 
@@ -348,6 +479,32 @@ int attn_fwd_kv_static(const void* q, const void* k, const void* v, void* o, flo
     if (!scratch) return cuda_fail(e);
     return fwd_kv_impl(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, scratch, kStaticScratchBytes,
                        stream);
+}
+
+size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    if (B > INT32_MAX || H > INT32_MAX || N > INT32_MAX || B * H > INT32_MAX) return 0;
+    if (B * H > (int64_t(1) << 60) / (N * d)) return 0;
+    return static_cast<size_t>(bwd_layout(B * H, N, d).bytes);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+             int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    const BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, dtype, workspace,
+                    workspace_bytes, stream};
+    return bwd_impl(a);
+}
+
+int attn_bwd_checked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
+                     int64_t d, int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+    BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, dtype, workspace,
+              workspace_bytes, stream};
+    const int st = bwd_validate(a);
+    if (st != ATTN_OK) return st;
+    return checked(run_bwd, &a, q, stream);
 }
 
 const char* attn_strerror(int status) {

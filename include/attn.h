@@ -152,6 +152,52 @@ int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, fl
 size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d);
 
 /*
+ * attn_bwd -- enqueue the backward pass on `stream`: the gradients of sum(dO * O)
+ * with respect to q, k and v for the forward defined at the top of this header
+ * (same mask and scale), from the forward's o and lse.
+ *
+ *   P_ij = exp(scale q_i.k_j - LSE_i) over the visible keys, D_i = dO_i . O_i,
+ *   dV_j = sum_i P_ij dO_i,   dS_ij = P_ij (dO_i . v_j - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i.
+ *
+ * Sources: "如何用 profiler 逐步优化 Triton FlashAttention-2 kernel", "Future
+ * articles", names the FA2 backward as the next kernel, one that consumes the L
+ * the forward saves ("Round 4 / exp2": natural-log units) and accumulates in two
+ * directions; the forward there is a torch.autograd.Function, so the backward is
+ * the chain rule through the definition.
+ *
+ *  - q, k, v, o, dout: DEVICE [B, H, N, d] of `dtype`, read only; lse: DEVICE
+ *    [B, H, N] fp32 from attn_fwd with the same q, k, v, causal and scale.
+ *  - dq, dk, dv: DEVICE [B, H, N, d] of `dtype`, written (rounded once from fp32).
+ *  - workspace: DEVICE scratch owned by the caller, at least
+ *    attn_bwd_workspace_bytes(B, H, N, d) bytes (fp32 D and LSE vectors and the
+ *    dQ accumulator); nothing in it needs to be initialised. Calls that may run
+ *    at the same time need workspaces of their own.
+ *  - All ten pointers 16-byte aligned; the outputs and the workspace must not
+ *    overlap each other or any input. Sizes and scale as for attn_fwd.
+ *  - dQ is summed over key tiles with fp32 atomic additions, so its last bits
+ *    may differ from run to run; dK and dV are deterministic.
+ *  - Returns ATTN_OK once the three kernels are enqueued, or an error status
+ *    with nothing enqueued (ATTN_ERR_INVALID_ARG also for a short workspace).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H,
+             int64_t N, int64_t d, int causal, float scale, int dtype, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/* attn_bwd_checked -- attn_bwd, then synchronise and read the device status
+ * word, as attn_fwd_checked. */
+int attn_bwd_checked(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                     int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_bwd_workspace_bytes -- workspace attn_bwd needs for these sizes: 8 bytes per
+ * row padded to 128 rows, plus 4*d bytes per row (0 for sizes attn_bwd rejects).
+ * Pure host arithmetic, no CUDA call. */
+size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
+
+/*
  * attn_fwd_kv_static -- attn_fwd_kv that allocates nothing and takes no
  * workspace: the split partials go to a static device array of 8 MiB
  * (8388608 bytes) inside this library. The

@@ -93,7 +93,8 @@ def test_probe_validation(lib):
 
 def test_headers_declare_the_kv_forward():
     names = _declared_symbols()
-    for n in ("attn_fwd_kv", "attn_fwd_kv_checked", "attn_fwd_kv_workspace_bytes"):
+    for n in ("attn_fwd_kv", "attn_fwd_kv_checked", "attn_fwd_kv_workspace_bytes", "attn_bwd",
+              "attn_bwd_checked", "attn_bwd_workspace_bytes"):
         assert n in names
 
 
@@ -176,3 +177,38 @@ def test_static_scratch_entry_rejects_before_any_cuda_call(lib):
     for BH in (1, 7, 100, 151, 152, 303):
         for d in (64, 128):
             assert attn.workspace_bytes(1, BH, 16, 1 << 20, d) <= attn.STATIC_SCRATCH_BYTES
+
+
+def _call_bwd(attn, checked=False, **kw):
+    M = 64 * A  # 64 MiB apart: room for every tensor of the default sizes
+    args = dict(q=1 * M, k=2 * M, v=3 * M, o=4 * M, lse=5 * M, dout=6 * M, dq=7 * M, dk=8 * M,
+                dv=9 * M, B=1, H=2, N=300, d=64, causal=1, scale=0.125, dtype=1, workspace=10 * M,
+                workspace_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return attn.attn_bwd(**args, checked=checked)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), 1), (dict(dout=0), 1), (dict(dq=0), 1), (dict(workspace=0), 1),
+    (dict(N=0), 1), (dict(dtype=3), 1), (dict(scale=-1.0), 1),
+    (dict(d=32), 2), (dict(B=1 << 31), 2),
+    (dict(dk=8 * 64 * A + 8), 3), (dict(lse=5 * 64 * A + 4), 3), (dict(workspace=10 * 64 * A + 2), 3),
+    (dict(workspace_bytes=100), 1),          # short workspace
+    (dict(dq=64 * A), 1),                    # dq aliases q
+    (dict(dk=7 * 64 * A), 1),                # dk aliases dq
+    (dict(dv=64 * A + 4096), 1),             # dv inside q
+    (dict(workspace=9 * 64 * A + 1024), 1),  # workspace overlaps dv
+])
+def test_bwd_host_validation(lib, kw, status):
+    from exact_attention_61_gb300 import attn
+    assert _call_bwd(attn, **kw) == status
+    assert _call_bwd(attn, checked=True, **kw) == status
+
+
+def test_bwd_workspace_bytes(lib):
+    from exact_attention_61_gb300 import attn
+    # 8 bytes per row padded to 128 rows (LSE, D) + 4 d bytes per row (dQ accumulator)
+    assert attn.bwd_workspace_bytes(1, 2, 300, 64) == 2 * 384 * 8 + 2 * 300 * 64 * 4
+    assert attn.bwd_workspace_bytes(4, 16, 4096, 128) == 64 * 4096 * 8 + 64 * 4096 * 128 * 4
+    assert attn.bwd_workspace_bytes(1, 1, 1, 96) == 0
+    assert attn.bwd_workspace_bytes(0, 1, 128, 64) == 0

@@ -119,3 +119,12 @@ def test_decode_bytes():
     for w in DECODE_WORKLOADS:
         assert decode_workload(w.name) is w
     assert bench.parse_args(["--decode", "b8h32q1k8192d128"]).decode == "b8h32q1k8192d128"
+
+
+def test_bwd_flops():
+    import bench
+    from exact_attention_61_gb300 import counts
+    # five N x N x d products against the forward's two
+    assert bench.bwd_flops(4, 16, 4096, 64, False) == 2.5 * counts.attn_flops(4, 16, 4096, 64, False)
+    assert bench.bwd_flops(4, 16, 4096, 64, True) == 2.5 * counts.attn_flops(4, 16, 4096, 64, True)
+    assert bench.parse_args(["--bwd"]).bwd
