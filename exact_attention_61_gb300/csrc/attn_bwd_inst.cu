@@ -28,7 +28,7 @@ cudaError_t launch_bwd_one(const CUtensorMap* m, const BwdParams& p, cudaStream_
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const unsigned grid = static_cast<unsigned>(p.n_tiles) * static_cast<unsigned>(p.BH);
-    kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], p);
+    kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], p);
     return cudaGetLastError();
 }
 

@@ -44,7 +44,8 @@ struct BwdConvertParams {
     long long n;          // BH * N * d
 };
 
-// maps: Q, K, V, dO (3-D [BH][N][d] 16-bit, 64 x 128 boxes, 128-byte swizzle).
+// maps: Q, K, V, dO (3-D [BH][N][d] 16-bit, 64 x 128 boxes, 128-byte swizzle), then the
+// fp32 dQ accumulator (3-D [BH][N][d], 32 x 128 boxes, 128-byte swizzle).
 cudaError_t launch_bwd_d64_f16(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd_d64_bf16(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd_d128_f16(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);

@@ -23,11 +23,12 @@
 //      dV  += P^T dO    (P^T 16-bit in TMEM over S^T; dO MN-major in SMEM)
 //      dK  += dS^T Q    (dS^T 16-bit in TMEM over dP^T; Q MN-major in SMEM)
 //      dQ   = dS K      (dS 16-bit in SMEM, MN-major; K MN-major in SMEM)
-//  - one warpgroup, one thread per key row (= TMEM lane), turns S^T and dP^T
-//    into P^T and dS^T with exp2 and the LSE folded in log2 units, writes dS
-//    for the dQ product to shared memory, then adds the dQ tile into an fp32
-//    workspace with vector atomics (dQ gathers over key tiles owned by other
-//    CTAs);
+//  - two warpgroups, one thread per key row (= TMEM lane) and half of the 128
+//    query columns each, turn S^T and dP^T into P^T and dS^T with exp2 and the
+//    LSE folded in log2 units, and write dS for the dQ product to shared memory;
+//  - a third warpgroup adds each dQ tile into an fp32 workspace with vector
+//    atomics (dQ gathers over key tiles owned by other CTAs), off the critical
+//    path of the other two;
 //  - dK and dV stay in TMEM for the whole loop and are stored once at the end;
 //  - every mbarrier wait is bounded, as in the forward kernel.
 #pragma once
@@ -37,7 +38,7 @@
 
 namespace attn_sm103 {
 
-enum : uint32_t { kRoleBwdLoad = 5, kRoleBwdMma = 6, kRoleBwdCompute = 7 };
+enum : uint32_t { kRoleBwdLoad = 5, kRoleBwdMma = 6, kRoleBwdCompute = 7, kRoleBwdDq = 8 };
 constexpr uint32_t kErrSmemAlign = 2u;
 
 // ---- tcgen05 / bulk-copy forms only the backward uses ------------------------------------
@@ -70,6 +71,36 @@ __device__ __forceinline__ void mma_mn128_warp(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// D (+)= A B over 128 rows of K with A (16-bit) in TMEM stored as two halves: K rows
+// 0-63 in columns [a, a+32) and K rows 64-127 in [a+64, a+96) (each compute warpgroup
+// packs its half of the 128 fp32 columns in place). B MN-major in SMEM, advancing 16
+// rows = 128 descriptor units per MMA. `accumulate` applies to the first MMA.
+__device__ __forceinline__ void mma_pv128_halves_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                      uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, one;\n\t.reg .b32 ta;\n\t.reg .b64 bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 one, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.u64 bd, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.u64 bd, %2, 256;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.u64 bd, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 64;\n\tadd.u64 bd, %2, 512;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 72;\n\tadd.u64 bd, %2, 640;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 80;\n\tadd.u64 bd, %2, 768;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 88;\n\tadd.u64 bd, %2, 896;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor with the major-ness of A chosen too (bit 15; A from SMEM).
 __host__ __device__ constexpr uint32_t idesc_f16_f32acc_ab(bool bf16, int M, int N, bool a_mn_major,
                                                            bool b_mn_major) {
@@ -95,6 +126,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Shared -> global element-wise fp32 add of a 3-D box (bulk async-group completion).
+// Rows outside the tensor are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
+                                                  int32_t c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            map),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -114,7 +156,12 @@ struct BwdCfg {
     static constexpr int kOffDS = kOffV + kTileBytes;   // dS: 128 keys x 128 queries, MN-major
     static constexpr int kOffStage = kOffDS + 128 * 128 * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;  // Q, then dO
-    static constexpr int kOffVec = kOffStage + kStages * kStageBytes;
+    // d = 64: the dQ tile is staged (fp32, 2 boxes of 32 columns x 128 rows, 128-byte
+    // swizzle) and added to the accumulator by TMA; d = 128 has no room and uses atomics.
+    static constexpr bool kTmaDq = D == 64;
+    static constexpr int kOffDqStage = kOffStage + kStages * kStageBytes;
+    static constexpr int kDqBoxBytes = 128 * 32 * 4;
+    static constexpr int kOffVec = kOffDqStage + (kTmaDq ? 2 * kDqBoxBytes : 0);
     static constexpr int kVecBytes = 2 * 128 * 4;       // lse2[128], D[128] per stage
     static constexpr int kOffBar = kOffVec + kStages * kVecBytes;
     static constexpr int kBarKV = 0;
@@ -136,16 +183,19 @@ struct BwdCfg {
     static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
     static constexpr uint32_t colDQ = D == 64 ? 384u : 0u;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kThreads = 192;  // warps 0-3 compute, 4 MMA, 5 TMA
-    static constexpr int kWarpMma = 4;
-    static constexpr int kWarpLoad = 5;
+    // warps 0-3: compute, query columns 0-63; 4-7: compute, columns 64-127;
+    // 8-11: dQ read-out; 12: MMA; 13: TMA
+    static constexpr int kThreads = 448;
+    static constexpr int kWarpDq = 8;
+    static constexpr int kWarpMma = 12;
+    static constexpr int kWarpLoad = 13;
 };
 
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_bwd[];
     const uint32_t base = smem_addr(smem_bwd);
@@ -174,8 +224,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages) count = 1 + 4;  // MMA + 4 warps
-            if (i == C::kBarPds || i == C::kBarDqRead) count = 4;                        // one per warp
+            if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages) count = 1 + 8;  // MMA + compute warps
+            if (i == C::kBarPds) count = 8;                                              // compute warps
+            if (i == C::kBarDqRead) count = 4;                                           // dQ warps
             mbar_init(bar(i), count);
         }
         misc[1] = 0u;
@@ -280,8 +331,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            mma_pv128_warp(tmem + C::colDV, tmem + C::colS, do_mn, idesc_o, it > 0 ? 1u : 0u);
-            mma_pv128_warp(tmem + C::colDK, tmem + C::colDP, q_mn, idesc_o, it > 0 ? 1u : 0u);
+            mma_pv128_halves_warp(tmem + C::colDV, tmem + C::colS, do_mn, idesc_o, it > 0 ? 1u : 0u);
+            mma_pv128_halves_warp(tmem + C::colDK, tmem + C::colDP, q_mn, idesc_o, it > 0 ? 1u : 0u);
             // d = 64: the dQ columns of the previous iteration must have been read out.
             if (D == 64 && it > 0 &&
                 !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
@@ -298,14 +349,82 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_commit_warp(bar(C::kBarDrain));
         wait_warp(bar(C::kBarDrain), 0, wc, kRoleBwdMma * 1000 + C::kBarDrain, 0, false);
         __syncwarp();
+    } else if (warp >= C::kWarpDq) {
+        // ================================ dQ read-out ==================================
+        // TMEM lane r of the dQ tile is query q0 + r; the tile is added to the fp32
+        // accumulator (other CTAs add the other key tiles' parts): at d = 64 through a
+        // swizzled shared-memory stage and TMA reduce-add, at d = 128 with vector atomics.
+        const uint32_t wq = warp - C::kWarpDq;
+        const uint32_t r = wq * 32u + lane;
+        const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
+        const bool leader = warp == C::kWarpDq && lane == 0;
+        if (C::kTmaDq && leader) tma_prefetch_desc(&tmDQ);
+        for (int it = 0; it < n_it; ++it) {
+            if (!wait_warp(bar(C::kBarDqFull), it & 1, wc, kRoleBwdDq * 1000 + C::kBarDqFull, it)) break;
+            tc_fence_after_sync();
+            const int q0 = (qt0 + it) * 128;
+            const int qrow = q0 + static_cast<int>(r);
+            if constexpr (C::kTmaDq) {
+                uint32_t o[2][32];
+                tmem_ld32(lane_base + C::colDQ, o[0]);
+                tmem_ld32(lane_base + C::colDQ + 32, o[1]);
+                tmem_ld_wait();
+                reg_fence(o[0]);
+                reg_fence(o[1]);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarDqRead));  // the dQ columns are free
+                // The previous tile's reduce has finished reading the stage.
+                if (leader) tma_store_wait_read_all();
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const uint32_t row = base + C::kOffDqStage + b * C::kDqBoxBytes + r * 128u;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(row + ((ch ^ (r & 7u)) << 4), o[b][4 * ch], o[b][4 * ch + 1], o[b][4 * ch + 2],
+                                     o[b][4 * ch + 3]);
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (leader && *wc.abort == 0u) {
+                    tma_reduce_add_3d(&tmDQ, base + C::kOffDqStage, 0, q0, bh);
+                    tma_reduce_add_3d(&tmDQ, base + C::kOffDqStage + C::kDqBoxBytes, 32, q0, bh);
+                    tma_store_commit();
+                }
+            } else {
+                float* dst = p.dq_acc + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + C::colDQ + 32 * c, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+                    if (qrow < N) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + e),
+                                      make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                                  __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarDqRead));
+            }
+        }
+        // Every reduce is complete in global memory before the CTA exits.
+        if (C::kTmaDq && leader) tma_store_wait_all();
     } else {
-        // ================================ compute warpgroup ===========================
-        const uint32_t wq = warp;                    // TMEM lane quarter
+        // ================================ compute warpgroups ==========================
+        // Warpgroup h handles query columns [64h, 64h + 64) of S^T and dP^T.
+        const uint32_t h = warp >> 2;
+        const uint32_t wq = warp & 3u;               // TMEM lane quarter
         const uint32_t r = wq * 32u + lane;          // key row in the tile = TMEM lane
         const int j = j0 + static_cast<int>(r);      // this thread's key
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
         const float qk = p.qk_scale;
-        const uint32_t sDS = base + C::kOffDS;
+        const uint32_t sDS = base + C::kOffDS + h * C::kBoxBytes + r * 128u;
         bool ok = true;
         for (int it = 0; it < n_it && ok; ++it) {
             const int s = it % C::kStages;
@@ -316,42 +435,47 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 ok = false;
                 break;
             }
+            // S^T(it) and dP^T(it) complete also means the dQ product of the previous
+            // iteration (issued before them) has finished reading the dS tile.
             tc_fence_after_sync();
             const float* vec = reinterpret_cast<const float*>(smem_bwd + C::kOffVec + s * C::kVecBytes);
-            const float* lse2 = vec;
-            const float* dvec = vec + 128;
+            const float* lse2 = vec + 64 * h;
+            const float* dvec = vec + 128 + 64 * h;
             const bool diag = CAUSAL && q0 == j0;  // only this Q tile has keys after queries
             const bool key_out = j >= N;           // padded key row: P = 0
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t col32 = 64u * h + 32u * c;  // first fp32 column of this chunk
                 uint32_t sr[32], dr[32];
-                tmem_ld32(lane_base + C::colS + 32 * c, sr);
-                tmem_ld32(lane_base + C::colDP + 32 * c, dr);
+                tmem_ld32(lane_base + C::colS + col32, sr);
+                tmem_ld32(lane_base + C::colDP + col32, dr);
                 tmem_ld_wait();
                 reg_fence(sr);
                 reg_fence(dr);
                 uint32_t pk[16], dk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const int col = 32 * c + e;
+                    const int col = 32 * c + e;                     // within this half
+                    const int qcol = 64 * static_cast<int>(h) + col;  // within the Q tile
                     float p0 = ex2_ftz(fmaf(__uint_as_float(sr[e]), qk, -lse2[col]));
                     float p1 = ex2_ftz(fmaf(__uint_as_float(sr[e + 1]), qk, -lse2[col + 1]));
-                    if (key_out || (diag && static_cast<int>(r) > col)) p0 = 0.f;
-                    if (key_out || (diag && static_cast<int>(r) > col + 1)) p1 = 0.f;
+                    if (key_out || (diag && static_cast<int>(r) > qcol)) p0 = 0.f;
+                    if (key_out || (diag && static_cast<int>(r) > qcol + 1)) p1 = 0.f;
                     const float ds0 = p0 * (__uint_as_float(dr[e]) - dvec[col]);
                     const float ds1 = p1 * (__uint_as_float(dr[e + 1]) - dvec[col + 1]);
                     pk[e >> 1] = pack2<BF16>(p0, p1);
                     dk[e >> 1] = pack2<BF16>(ds0, ds1);
                 }
-                tmem_st16(lane_base + C::colS + 16 * c, pk);
-                tmem_st16(lane_base + C::colDP + 16 * c, dk);
+                // 16-bit P^T / dS^T packed in place: half h lives in columns
+                // [64h, 64h + 32), chunk c in its 16 columns (already read above).
+                tmem_st16(lane_base + C::colS + 64u * h + 16u * c, pk);
+                tmem_st16(lane_base + C::colDP + 64u * h + 16u * c, dk);
                 // dS for the dQ product: element (query m, key r) of an MN-major operand,
-                // 128-byte swizzle; queries 32c..32c+31 are 4 chunks of 8 in row r.
-                const uint32_t blk = sDS + (c >> 1) * C::kBoxBytes + r * 128u;
+                // 128-byte swizzle; half h is box h, chunk c its 16-byte chunks 4c..4c+3.
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const uint32_t chunk = (c & 1) * 4u + t;
-                    st_shared_v4(blk + ((chunk ^ (r & 7u)) << 4), dk[4 * t], dk[4 * t + 1], dk[4 * t + 2],
+                    const uint32_t chunk = 4u * c + t;
+                    st_shared_v4(sDS + ((chunk ^ (r & 7u)) << 4), dk[4 * t], dk[4 * t + 1], dk[4 * t + 2],
                                  dk[4 * t + 3]);
                 }
             }
@@ -363,33 +487,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 mbar_arrive(bar(C::kBarPds));
                 mbar_arrive(bar(C::kBarQdEmpty + s));
             }
-            // dQ tile: TMEM lane r is query q0 + r.
-            if (!wait_warp(bar(C::kBarDqFull), it & 1, wc, kRoleBwdCompute * 1000 + C::kBarDqFull, it)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            const int qrow = q0 + static_cast<int>(r);
-            float* dst = p.dq_acc + (static_cast<size_t>(bh) * N + qrow) * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + C::colDQ + 32 * c, o);
-                tmem_ld_wait();
-                reg_fence(o);
-                if (qrow < N) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + e),
-                                  make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                              __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
-                }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarDqRead));
         }
-        // ---- epilogue: dV and dK rows of this thread's key ----------------------------
+        // ---- epilogue: dV and dK of this thread's key, columns [d/2 h, d/2 (h+1)) -----
         if (ok) ok = wait_warp(bar(C::kBarAcc), 0, wc, kRoleBwdCompute * 1000 + C::kBarAcc, n_it);
         if (ok) {
             tc_fence_after_sync();
@@ -399,7 +498,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 const float mul = which == 0 ? 1.f : p.scale;
                 uint8_t* out = static_cast<uint8_t*>(which == 0 ? p.dv : p.dk);
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
                     uint32_t o[32];
                     tmem_ld32(lane_base + col + 32 * c, o);
                     tmem_ld_wait();

@@ -373,19 +373,31 @@ int bwd_impl(const BwdArgs& a) {
     if (!status) return cuda_fail(e);
     const int64_t BH = a.B * a.H;
     const BwdLayout L = bwd_layout(BH, a.N, a.d);
-    alignas(64) CUtensorMap maps[4];
+    char* ws = static_cast<char*>(a.ws);
+    float* lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
+    float* dvec = reinterpret_cast<float*>(ws + L.dvec_off);
+    float* dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
+    alignas(64) CUtensorMap maps[5];
     const void* ptrs[4] = {a.q, a.k, a.v, a.dout};
-    for (int i = 0; i < 4; ++i) {
-        const CUresult r = make_map(enc, &maps[i], ptrs[i], BH, a.N, a.d, a.dtype);
+    for (int i = 0; i < 5; ++i) {
+        CUresult r;
+        if (i < 4) {
+            r = make_map(enc, &maps[i], ptrs[i], BH, a.N, a.d, a.dtype);
+        } else {  // fp32 dQ accumulator, 32-column boxes (128 bytes: the swizzle span)
+            const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.d), static_cast<cuuint64_t>(a.N),
+                                        static_cast<cuuint64_t>(BH)};
+            const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.d * 4), static_cast<cuuint64_t>(a.N * a.d * 4)};
+            const cuuint32_t box[3] = {32, 128, 1};
+            const cuuint32_t estr[3] = {1, 1, 1};
+            r = enc(&maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
         if (r != CUDA_SUCCESS) {
             g_last_cuda_error = 100000 + static_cast<int>(r);
             return ATTN_ERR_CUDA;
         }
     }
-    char* ws = static_cast<char*>(a.ws);
-    float* lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
-    float* dvec = reinterpret_cast<float*>(ws + L.dvec_off);
-    float* dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
     const bool bf16 = a.dtype == ATTN_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(a.stream);
 
