@@ -82,6 +82,9 @@ def _load():
                                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                ctypes.c_int, ctypes.c_double]
             lib.oracle_attn_fwd_qk.restype = ctypes.c_int
+            lib.oracle_attn_fwd_window.argtypes = [_DP, _DP, _DP, _DP, _DP] + [ctypes.c_int64] * 7 + [
+                _I64P, ctypes.c_int, ctypes.c_double]
+            lib.oracle_attn_fwd_window.restype = ctypes.c_int
             lib.oracle_attn_bwd.argtypes = [_DP, _DP, _DP, _DP, _DP, _DP, _DP, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                             ctypes.c_double]
@@ -305,3 +308,49 @@ def attn_bwd_materialised(q, k, v, dout, causal: bool, scale: float | None = Non
         "dv": np.einsum("bhij,bhid->bhjd", p, g64),
         "p": p, "dp": dp, "ds": ds, "D": D[..., 0],
     }
+
+
+def attn_fwd_window(q, k, v, left: int = -1, right: int = -1, kv_lens=None, align: str = "top_left",
+                    scale: float | None = None):
+    """Nq query rows [B,H,Nq,d] against Nk keys [B,H,Nk,d] with a sliding window and key
+    padding (C, fp64).
+
+    Batch element b has ``kv_lens[b]`` valid keys (None: all). Row i's diagonal is key
+    i + off_b with off_b = 0 (``align="top_left"``) or kv_lens[b] - Nq
+    (``"bottom_right"``); it sees valid keys diag - left <= j <= diag + right, a negative
+    bound meaning unbounded on that side (right = 0 is the causal mask). Rows that see no
+    key get O = 0 and LSE = -inf. Returns (O [B,H,Nq,d], LSE [B,H,Nq]).
+    """
+    q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
+    B, H, Nq, d = q64.shape
+    Nk = k64.shape[2]
+    if k64.shape != (B, H, Nk, d) or v64.shape != k64.shape:
+        raise ValueError("q [B,H,Nq,d], k and v [B,H,Nk,d] must agree on B, H, d")
+    scale = default_scale(d) if scale is None else float(scale)
+    lens = None
+    if kv_lens is not None:
+        lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int64).reshape(B))
+    o = np.empty_like(q64)
+    lse = np.empty((B, H, Nq), dtype=np.float64)
+    rc = _load().oracle_attn_fwd_window(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(o), _ptr(lse), B, H, Nq,
+                                        Nk, d, int(left), int(right),
+                                        lens.ctypes.data_as(_I64P) if lens is not None else None,
+                                        {"top_left": 0, "bottom_right": 1}[align], scale)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_window failed with code {rc}")
+    return o, lse
+
+
+def window_mask(B, Nq, Nk, left=-1, right=-1, kv_lens=None, align="top_left"):
+    """Boolean [B, Nq, Nk] visibility of :func:`attn_fwd_window`, spelled out in numpy."""
+    lens = np.full(B, Nk) if kv_lens is None else np.asarray(kv_lens).reshape(B)
+    i = np.arange(Nq)[None, :, None]
+    j = np.arange(Nk)[None, None, :]
+    n = lens[:, None, None]
+    diag = i + (n - Nq if align == "bottom_right" else 0)
+    keep = j < n
+    if left >= 0:
+        keep = keep & (j >= diag - left)
+    if right >= 0:
+        keep = keep & (j <= diag + right)
+    return keep

@@ -213,6 +213,64 @@ int oracle_attn_fwd_qk(const double* q, const double* k, const double* v, double
     return failed ? -2 : 0;
 }
 
+/* Sliding windows and key padding, for Nq query rows against Nk keys. The
+ * profile-driven FlashAttention-2 page ("Future articles") names padding masks and
+ * sliding windows as the kernels in which a row can be fully masked; it defines
+ * neither, so the plainest readings are taken:
+ *  - key padding: batch element b has kv_lens[b] valid keys (0 <= kv_lens[b] <= Nk;
+ *    NULL = all Nk), the right-padded layout of a batch of different lengths;
+ *  - the diagonal of row i is key i + off_b, with off_b = 0 (top-left, align = 0)
+ *    or off_b = n_b - Nq (bottom-right, align = 1: the query rows are the last Nq
+ *    positions of each sequence), n_b the valid key count of its batch element;
+ *  - a sliding window keeps keys i + off_b - left <= j <= i + off_b + right
+ *    (left or right < 0: unbounded on that side; right = 0 is the causal mask).
+ * Row i of batch element b sees keys j with 0 <= j < n_b inside the window. A row
+ * that sees none gets O = 0 and LSE = -inf. */
+int oracle_attn_fwd_window(const double* q, const double* k, const double* v, double* o,
+                           double* lse, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                           int64_t left, int64_t right, const int64_t* kv_lens, int align,
+                           double scale)
+{
+    if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return -1;
+    if (!(scale > 0.0) || !isfinite(scale)) return -1;
+    if (kv_lens)
+        for (int64_t b = 0; b < B; ++b)
+            if (kv_lens[b] < 0 || kv_lens[b] > Nk) return -1;
+    int failed = 0;
+#pragma omp parallel reduction(| : failed)
+    {
+        double* s = (double*)malloc((size_t)Nk * sizeof(double));
+        if (!s) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4) collapse(2)
+            for (int64_t bh = 0; bh < B * H; ++bh) {
+                for (int64_t i = 0; i < Nq; ++i) {
+                    const int64_t n_b = kv_lens ? kv_lens[bh / H] : Nk;
+                    const int64_t diag = i + (align ? n_b - Nq : 0);
+                    int64_t lo = left < 0 ? 0 : diag - left;
+                    int64_t hi = right < 0 ? n_b - 1 : diag + right;
+                    if (lo < 0) lo = 0;
+                    if (hi > n_b - 1) hi = n_b - 1;
+                    const double* qi = q + (bh * Nq + i) * d;
+                    double* oi = o + (bh * Nq + i) * d;
+                    double* li = lse + bh * Nq + i;
+                    if (hi < lo) {
+                        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+                        *li = -INFINITY;
+                        continue;
+                    }
+                    /* keys lo..hi of this head: the row routine over a shifted block */
+                    oracle_row_n(qi, k + (bh * Nk + lo) * d, v + (bh * Nk + lo) * d, d, hi - lo + 1,
+                                 scale, s, oi, li);
+                }
+            }
+            free(s);
+        }
+    }
+    return failed ? -2 : 0;
+}
+
 /* Backward of the forward above: the vector-Jacobian product of O = attn(Q, K, V)
  * with an upstream gradient dO, i.e. the gradients of sum(dO * O) with respect to
  * Q, K and V. "如何用 profiler 逐步优化 Triton FlashAttention-2 kernel", "Future
