@@ -47,6 +47,11 @@ _FWD_KV_ARGS = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void
                 ctypes.c_void_p]
 
 
+_WIN_ARGS = ([ctypes.c_void_p] * 5 + [ctypes.c_int64] * 7 +
+             [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
+              ctypes.c_size_t, ctypes.c_void_p])
+ALIGN = {"top_left": 0, "bottom_right": 1}
+
 _BWD_ARGS = ([ctypes.c_void_p] * 9 + [ctypes.c_int64] * 4 +
              [ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
               ctypes.c_void_p])
@@ -80,6 +85,10 @@ def load(path: str = LIB_PATH):
             lib.attn_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_fwd_kv_static.argtypes = _FWD_KV_ARGS[:13] + [ctypes.c_void_p]
             lib.attn_fwd_kv_static.restype = ctypes.c_int
+            lib.attn_fwd_window.argtypes = _WIN_ARGS
+            lib.attn_fwd_window.restype = ctypes.c_int
+            lib.attn_fwd_window_checked.argtypes = _WIN_ARGS
+            lib.attn_fwd_window_checked.restype = ctypes.c_int
             lib.attn_bwd.argtypes = _BWD_ARGS
             lib.attn_bwd.restype = ctypes.c_int
             lib.attn_bwd_checked.argtypes = _BWD_ARGS
@@ -233,6 +242,54 @@ def fwd_kv(q, k, v, mask: str = "none", scale: Optional[float] = None, out=None,
                      Nq, Nk, d, MASKS[mask], scale, _dtype_code(q), ws_ptr, ws_n, stream.cuda_stream,
                      checked=checked)
     _check(st, "attn_fwd_kv")
+    return out, lse
+
+
+def attn_fwd_window(q, k, v, o, lse, B, H, Nq, Nk, d, window_left, window_right, kv_lens, align, scale,
+                    dtype, workspace, workspace_bytes, stream, checked: bool = False) -> int:
+    """Raw C call of attn_fwd_window (or its checked form); returns the attn_status_t."""
+    lib = load()
+    fn = lib.attn_fwd_window_checked if checked else lib.attn_fwd_window
+    return int(fn(q, k, v, o, lse, B, H, Nq, Nk, d, int(window_left), int(window_right), kv_lens,
+                  int(align), float(scale), int(dtype), workspace, int(workspace_bytes), stream))
+
+
+def fwd_window(q, k, v, window=(-1, -1), kv_lens=None, align: str = "top_left",
+               scale: Optional[float] = None, out=None, lse=None, workspace=None, stream=None,
+               checked: bool = False):
+    """Forward of q [B,H,Nq,d] against k, v [B,H,Nk,d] with a sliding window
+    ``(left, right)`` around the diagonal (negative: unbounded; right = 0 is causal) and
+    optional per-batch valid key counts ``kv_lens`` (CUDA int32 [B]). Rows that see no
+    key get O = 0 and LSE = -inf. Returns (o, lse)."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] must agree on B, H and d")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if kv_lens is not None:
+        if kv_lens.dtype != torch.int32 or kv_lens.shape != (B,) or not kv_lens.is_cuda:
+            raise ValueError("kv_lens must be a CUDA int32 tensor of shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        n = workspace_bytes(B, H, Nq, Nk, d)
+        workspace = torch.empty((n,), dtype=torch.uint8, device=q.device) if n else False
+    ws_ptr, ws_n = (workspace.data_ptr(), workspace.numel()) if workspace is not False else (None, 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq,
+                         Nk, d, window[0], window[1], kv_lens.data_ptr() if kv_lens is not None else None,
+                         ALIGN[align], scale, _dtype_code(q), ws_ptr, ws_n, stream.cuda_stream, checked=checked)
+    _check(st, "attn_fwd_window")
     return out, lse
 
 

@@ -13,10 +13,10 @@
 namespace attn_sm103 {
 namespace {
 
-template <int D, bool CAUSAL, bool BF16, bool SPLIT>
+template <int D, bool CAUSAL, bool BF16, bool SPLIT, bool EXT>
 cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s) {
     using C = FwdCfg<D>;
-    auto* kern = attn_fwd_kernel<D, CAUSAL, BF16, SPLIT>;
+    auto* kern = attn_fwd_kernel<D, CAUSAL, BF16, SPLIT, EXT>;
     // The dynamic shared-memory opt-in is per device; remember which devices have it.
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -45,14 +45,22 @@ cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s)
 #endif
 #define ATTN_LAUNCH_NAME ATTN_CAT(ATTN_CAT(ATTN_CAT(launch_fwd_d, ATTN_INST_D), _), ATTN_DT_SUFFIX)
 
-cudaError_t ATTN_LAUNCH_NAME(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p,
+cudaError_t ATTN_LAUNCH_NAME(bool causal, bool split, bool ext, const CUtensorMap* maps, const FwdParams& p,
                              cudaStream_t s) {
     constexpr bool kBf16 = ATTN_INST_BF16 != 0;
+    constexpr int kD = ATTN_INST_D;
+    if (ext) {
+        if (split)
+            return causal ? launch_one<kD, true, kBf16, true, true>(maps, p, s)
+                          : launch_one<kD, false, kBf16, true, true>(maps, p, s);
+        return causal ? launch_one<kD, true, kBf16, false, true>(maps, p, s)
+                      : launch_one<kD, false, kBf16, false, true>(maps, p, s);
+    }
     if (split)
-        return causal ? launch_one<ATTN_INST_D, true, kBf16, true>(maps, p, s)
-                      : launch_one<ATTN_INST_D, false, kBf16, true>(maps, p, s);
-    return causal ? launch_one<ATTN_INST_D, true, kBf16, false>(maps, p, s)
-                  : launch_one<ATTN_INST_D, false, kBf16, false>(maps, p, s);
+        return causal ? launch_one<kD, true, kBf16, true, false>(maps, p, s)
+                      : launch_one<kD, false, kBf16, true, false>(maps, p, s);
+    return causal ? launch_one<kD, true, kBf16, false, false>(maps, p, s)
+                  : launch_one<kD, false, kBf16, false, false>(maps, p, s);
 }
 
 }  // namespace attn_sm103

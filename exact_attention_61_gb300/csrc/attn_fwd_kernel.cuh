@@ -36,6 +36,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <climits>
+
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -217,7 +219,9 @@ __device__ __forceinline__ float row_max128(const uint32_t (&sr)[4][32]) {
 
 // SPLIT: this CTA covers key tiles [blockIdx.y * tiles_per_split, ...) only and writes
 // fp32 partials (O_s = O/l and log2-sum-exp) instead of O and LSE.
-template <int D, bool CAUSAL, bool BF16, bool SPLIT>
+// EXT: per-batch valid key counts, a left window bound and a right bound other than the
+// diagonal; without it those parameters are ignored and the code is not compiled in.
+template <int D, bool CAUSAL, bool BF16, bool SPLIT, bool EXT>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -240,14 +244,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     // ---- which rows this CTA owns (heaviest causal tiles are launched first) --------
     const int bh = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.BH));
     const int ct = p.n_ctiles - 1 - static_cast<int>(blockIdx.x / static_cast<uint32_t>(p.BH));
-    const int Nq = p.Nq, Nk = p.Nk;
-    // Under the causal mask row i sees keys j <= i + off: off = 0 aligns the first query
-    // row with the first key (top-left), off = Nk - Nq makes the query rows the last Nq
-    // positions of the key sequence (bottom-right, as in decoding).
-    const int off = p.causal_off;
+    const int Nq = p.Nq;
+    // Valid keys of this batch element (key padding): the first Nk of its keys.
+    const int Nk = (EXT && p.kv_lens) ? min(max(p.kv_lens[bh / p.H], 0), p.Nk) : p.Nk;
+    // The diagonal of row i is key i (top-left) or i + Nk - Nq (bottom-right: the query
+    // rows are the last Nq positions, as in decoding). Under the causal mask row i sees
+    // keys j <= i + off; with a left window only keys j >= i + lo_off.
+    const int diag = p.align_br ? Nk - Nq : 0;
+    const int off = diag + (EXT ? p.win_right : 0);
+    const bool has_lo = EXT && p.win_left >= 0;
+    const int lo_off = diag - p.win_left;
     const int n_kv_all = (Nk + C::BN - 1) / C::BN;
-    const int kv_begin = SPLIT ? static_cast<int>(blockIdx.y) * p.tiles_per_split : 0;
+    int kv_begin = SPLIT ? static_cast<int>(blockIdx.y) * p.tiles_per_split : 0;
     const int kv_end = SPLIT ? min(n_kv_all, kv_begin + p.tiles_per_split) : n_kv_all;
+    // Key tiles wholly left of the first row's window are never visited. The second Q
+    // tile starts with the first (at most one extra, fully masked tile for it).
+    if (has_lo) {
+        const int first_key = ct * C::kRowsPerCta + lo_off;
+        if (first_key > 0) kv_begin = max(kv_begin, first_key / C::BN);
+    }
     // First query row and number of key tiles of each Q tile (kept in scalars: an
     // array indexed by the tile would live in local memory).
     // Key tiles a Q tile needs: all of [kv_begin, kv_end), or, under the causal mask,
@@ -441,14 +456,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
 
             const int k0 = (kv_begin + j) * C::BN;
-            const bool need_mask = (k0 + C::BN > Nk) || (CAUSAL && k0 + C::BN - 1 > row0(t) + off);
+            const bool need_mask = (k0 + C::BN > Nk) || (CAUSAL && k0 + C::BN - 1 > row0(t) + off) ||
+                                   (has_lo && k0 < row0(t) + C::BM - 1 + lo_off);
             if (need_mask) {
-                const int lim = CAUSAL ? min(Nk, q_row + off + 1) : Nk;  // keys below lim are visible
+                // keys in [lim_lo, lim) are visible
+                const int lim = CAUSAL ? min(Nk, q_row + off + 1) : Nk;
+                const int lim_lo = has_lo ? q_row + lo_off : INT_MIN;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (k0 + c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+                    for (int e = 0; e < 32; ++e) {
+                        const int key = k0 + c * 32 + e;
+                        if (key >= lim || key < lim_lo) sr[c][e] = __float_as_uint(-INFINITY);
+                    }
             }
             const float row_max = row_max128(sr);
             float m_new = fmaxf(m, row_max * qk);

@@ -199,11 +199,23 @@ SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_by
 
 namespace {
 
-int fwd_kv_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-                int64_t Nq, int64_t Nk, int64_t d, int mask, float scale, int dtype, void* ws,
-                size_t ws_bytes, void* stream) {
-    const int st = validate(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, ws, ws_bytes);
-    if (st != ATTN_OK) return st;
+// Which keys a row sees, beyond j < (valid keys of its batch element).
+struct MaskSpec {
+    bool causal;              // upper bound j <= diagonal + win_right
+    int align_br;             // diagonal of row i: i (0) or i + n_b - Nq (1)
+    int win_right;            // >= 0 when causal
+    int win_left;             // lower bound j >= diagonal - win_left, or < 0: none
+    const int32_t* kv_lens;   // device [B] valid keys, or null
+};
+
+MaskSpec mask_of(int mask) {
+    MaskSpec m{mask != ATTN_MASK_NONE, mask == ATTN_MASK_CAUSAL_BOTTOM_RIGHT ? 1 : 0, 0, -1, nullptr};
+    return m;
+}
+
+int fwd_core(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+             int64_t Nq, int64_t Nk, int64_t d, const MaskSpec& ms, float scale, int dtype, void* ws,
+             size_t ws_bytes, void* stream) {
     int dev = 0;
     cudaError_t e = select_device_of(q, &dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -233,18 +245,26 @@ int fwd_kv_impl(const void* q, const void* k, const void* v, void* o, float* lse
     p.BH = static_cast<int>(BH);
     p.n_ctiles = static_cast<int>((Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta);
     p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    p.causal_off = mask == ATTN_MASK_CAUSAL_BOTTOM_RIGHT ? static_cast<int>(Nk - Nq) : 0;
+    p.H = static_cast<int>(H);
+    p.kv_lens = ms.kv_lens;
+    p.align_br = ms.align_br;
+    p.win_right = ms.win_right;
+    p.win_left = ms.win_left;
     p.n_splits = static_cast<int>(plan.n_splits);
     p.tiles_per_split = static_cast<int>(plan.tiles_per_split);
     const bool split = plan.n_splits > 1;
     p.o_part = split ? static_cast<float*>(ws) : nullptr;
     p.lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.o_part_bytes) : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool c = mask != ATTN_MASK_NONE;
+    const bool c = ms.causal;
+    // Padding or a window other than the plain causal mask needs the extended instances.
+    const bool x = ms.kv_lens != nullptr || ms.win_left >= 0 || ms.win_right != 0;
     if (d == 64)
-        e = dtype == ATTN_BF16 ? launch_fwd_d64_bf16(c, split, maps, p, s) : launch_fwd_d64_f16(c, split, maps, p, s);
+        e = dtype == ATTN_BF16 ? launch_fwd_d64_bf16(c, split, x, maps, p, s)
+                               : launch_fwd_d64_f16(c, split, x, maps, p, s);
     else
-        e = dtype == ATTN_BF16 ? launch_fwd_d128_bf16(c, split, maps, p, s) : launch_fwd_d128_f16(c, split, maps, p, s);
+        e = dtype == ATTN_BF16 ? launch_fwd_d128_bf16(c, split, x, maps, p, s)
+                               : launch_fwd_d128_f16(c, split, x, maps, p, s);
     if (e != cudaSuccess) return cuda_fail(e);
     if (split) {
         MergeParams mp{p.o_part, p.lse_part, o, lse, p.BH, p.Nq, static_cast<int>(d), p.n_splits};
@@ -253,6 +273,60 @@ int fwd_kv_impl(const void* q, const void* k, const void* v, void* o, float* lse
     }
     return ATTN_OK;
 }
+
+int fwd_kv_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                int64_t Nq, int64_t Nk, int64_t d, int mask, float scale, int dtype, void* ws,
+                size_t ws_bytes, void* stream) {
+    const int st = validate(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, ws, ws_bytes);
+    if (st != ATTN_OK) return st;
+    return fwd_core(q, k, v, o, lse, B, H, Nq, Nk, d, mask_of(mask), scale, dtype, ws, ws_bytes, stream);
+}
+
+// Window bounds beyond Nq + Nk keys bind nothing: they become "unbounded" (-1).
+int window_spec(int64_t Nq, int64_t Nk, int64_t left, int64_t right, const int32_t* kv_lens, int align,
+                MaskSpec* out) {
+    if (align != ATTN_ALIGN_TOP_LEFT && align != ATTN_ALIGN_BOTTOM_RIGHT) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(kv_lens) % 4u) return ATTN_ERR_MISALIGNED;
+    if (Nq + Nk > (int64_t(1) << 30)) return ATTN_ERR_UNSUPPORTED;  // keeps i + offsets in int
+    const int64_t span = Nq + Nk;
+    out->align_br = align == ATTN_ALIGN_BOTTOM_RIGHT ? 1 : 0;
+    out->causal = right >= 0 && right < span;
+    out->win_right = out->causal ? static_cast<int>(right) : 0;
+    out->win_left = (left >= 0 && left < span) ? static_cast<int>(left) : -1;
+    out->kv_lens = kv_lens;
+    return ATTN_OK;
+}
+
+struct WinArgs {
+    const void *q, *k, *v;
+    void* o;
+    float* lse;
+    int64_t B, H, Nq, Nk, d, left, right;
+    const int32_t* kv_lens;
+    int align;
+    float scale;
+    int dtype;
+    void* ws;
+    size_t ws_bytes;
+    void* stream;
+};
+
+int win_validate(const WinArgs& a, MaskSpec* ms) {
+    const int st = validate(a.q, a.k, a.v, a.o, a.lse, a.B, a.H, a.Nq, a.Nk, a.d, ATTN_MASK_NONE, a.scale,
+                            a.dtype, a.ws, a.ws_bytes);
+    if (st != ATTN_OK) return st;
+    return window_spec(a.Nq, a.Nk, a.left, a.right, a.kv_lens, a.align, ms);
+}
+
+int win_impl(const WinArgs& a) {
+    MaskSpec ms;
+    const int st = win_validate(a, &ms);
+    if (st != ATTN_OK) return st;
+    return fwd_core(a.q, a.k, a.v, a.o, a.lse, a.B, a.H, a.Nq, a.Nk, a.d, ms, a.scale, a.dtype, a.ws, a.ws_bytes,
+                    a.stream);
+}
+
+int run_win(void* ctx) { return win_impl(*static_cast<const WinArgs*>(ctx)); }
 
 int checked(int (*run)(void*), void* ctx, const void* q, void* stream) {
     int dev = 0;
@@ -491,6 +565,27 @@ int attn_fwd_kv_static(const void* q, const void* k, const void* v, void* o, flo
     if (!scratch) return cuda_fail(e);
     return fwd_kv_impl(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, scratch, kStaticScratchBytes,
                        stream);
+}
+
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                    int64_t Nq, int64_t Nk, int64_t d, int64_t window_left, int64_t window_right,
+                    const int32_t* kv_lens, int align, float scale, int dtype, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    const WinArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, window_left, window_right, kv_lens, align, scale, dtype,
+                    workspace, workspace_bytes, stream};
+    return win_impl(a);
+}
+
+int attn_fwd_window_checked(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                            int64_t H, int64_t Nq, int64_t Nk, int64_t d, int64_t window_left,
+                            int64_t window_right, const int32_t* kv_lens, int align, float scale, int dtype,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    WinArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, window_left, window_right, kv_lens, align, scale, dtype,
+              workspace, workspace_bytes, stream};
+    MaskSpec ms;
+    const int st = win_validate(a, &ms);
+    if (st != ATTN_OK) return st;
+    return checked(run_win, &a, q, stream);
 }
 
 size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d) {

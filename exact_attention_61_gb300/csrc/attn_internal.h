@@ -18,7 +18,11 @@ struct FwdParams {
     int BH;           // batch * heads
     int n_ctiles;     // ceil(Nq / 256): CTA tiles per head
     float qk_scale;   // scale * log2(e), > 0
-    int causal_off;   // causal kernels: row i sees keys j <= i + causal_off
+    int H;            // heads (batch element of head bh is bh / H)
+    const int32_t* kv_lens;  // [B] valid keys per batch element (clamped to [0, Nk]), or null
+    int align_br;     // diagonal of row i: key i (0) or i + n_b - Nq (1, bottom-right)
+    int win_right;    // causal kernels: row i sees keys j <= diagonal + win_right
+    int win_left;     // >= 0: row i sees keys j >= diagonal - win_left; < 0: unbounded
     int tiles_per_split;  // key tiles per split (split s covers tiles [s*tps, (s+1)*tps))
     int n_splits;         // gridDim.y
     float* o_part;    // split mode: [BH][n_splits][Nq][d] fp32 partial outputs (O_s = O/l)
@@ -42,10 +46,14 @@ constexpr int kFwdRowsPerCta = 256;
 // attn_fwd_inst.cu; `causal` picks the template instance.
 // `split` selects the instance that writes fp32 partials (p.n_splits > 1); the
 // grid is (n_ctiles * BH, n_splits).
-cudaError_t launch_fwd_d64_f16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
-cudaError_t launch_fwd_d64_bf16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
-cudaError_t launch_fwd_d128_f16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
-cudaError_t launch_fwd_d128_bf16(bool causal, bool split, const CUtensorMap* maps, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_d64_f16(bool causal, bool split, bool ext, const CUtensorMap* maps, const FwdParams& p,
+                               cudaStream_t s);
+cudaError_t launch_fwd_d64_bf16(bool causal, bool split, bool ext, const CUtensorMap* maps, const FwdParams& p,
+                               cudaStream_t s);
+cudaError_t launch_fwd_d128_f16(bool causal, bool split, bool ext, const CUtensorMap* maps, const FwdParams& p,
+                               cudaStream_t s);
+cudaError_t launch_fwd_d128_bf16(bool causal, bool split, bool ext, const CUtensorMap* maps, const FwdParams& p,
+                               cudaStream_t s);
 cudaError_t launch_merge(bool bf16, const MergeParams& p, cudaStream_t s);
 
 // How the keys are split over CTAs (n_splits = 1: no split, no workspace).

@@ -62,6 +62,13 @@ typedef enum {
                                           rows are the last Nq positions (decoding)    */
 } attn_mask_t;
 
+/* Diagonal alignment of attn_fwd_window. */
+typedef enum {
+    ATTN_ALIGN_TOP_LEFT = 0,     /* row i's diagonal is key i                      */
+    ATTN_ALIGN_BOTTOM_RIGHT = 1  /* row i's diagonal is key i + n_b - Nq, n_b the
+                                    valid keys of its batch element                */
+} attn_align_t;
+
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* null pointer, size < 1, bad scale or dtype, overlap   */
@@ -150,6 +157,38 @@ int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, fl
  * its full split of the keys for these sizes (0: it never splits them). Pure
  * host arithmetic, no CUDA call; 0 for sizes attn_fwd_kv rejects. */
 size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d);
+
+/*
+ * attn_fwd_window -- attn_fwd_kv with a sliding window and key padding.
+ *
+ * Source: "如何用 profiler 逐步优化 Triton FlashAttention-2 kernel", "Future
+ * articles", names padding masks and sliding windows as the kernels in which a
+ * row can be fully masked (so a -inf sentinel must be handled); the page defines
+ * neither, and this call takes the plain readings:
+ *  - kv_lens: optional DEVICE int32 [B] (4-byte aligned; NULL = all Nk): batch
+ *    element b has n_b = kv_lens[b] valid keys, its first n_b (right padding).
+ *    Values are clamped to [0, Nk] on the device.
+ *  - align: an attn_align_t giving the diagonal of row i (i, or i + n_b - Nq).
+ *  - row i sees the valid keys j with diag - window_left <= j <= diag +
+ *    window_right; a negative bound (or one beyond Nq + Nk) is unbounded on that
+ *    side. window_right = 0 is the causal mask; (-1, -1) is no window.
+ *  - A row that sees no key gets O = 0 and LSE = -inf.
+ *  - Everything else (layouts, workspace and its split of the keys, errors) as
+ *    attn_fwd_kv. Nq + Nk must not exceed 2^30 (ATTN_ERR_UNSUPPORTED).
+ */
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                    int64_t window_left, int64_t window_right, const int32_t* kv_lens,
+                    int align, float scale, int dtype, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* attn_fwd_window_checked -- attn_fwd_window, then synchronise and read the device
+ * status word, as attn_fwd_checked. */
+int attn_fwd_window_checked(const void* q, const void* k, const void* v, void* o,
+                            float* lse, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                            int64_t d, int64_t window_left, int64_t window_right,
+                            const int32_t* kv_lens, int align, float scale, int dtype,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_bwd -- enqueue the backward pass on `stream`: the gradients of sum(dO * O)

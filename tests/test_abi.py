@@ -94,7 +94,8 @@ def test_probe_validation(lib):
 def test_headers_declare_the_kv_forward():
     names = _declared_symbols()
     for n in ("attn_fwd_kv", "attn_fwd_kv_checked", "attn_fwd_kv_workspace_bytes", "attn_bwd",
-              "attn_bwd_checked", "attn_bwd_workspace_bytes"):
+              "attn_bwd_checked", "attn_bwd_workspace_bytes", "attn_fwd_window",
+              "attn_fwd_window_checked"):
         assert n in names
 
 
@@ -212,3 +213,20 @@ def test_bwd_workspace_bytes(lib):
     assert attn.bwd_workspace_bytes(4, 16, 4096, 128) == 64 * 4096 * 8 + 64 * 4096 * 128 * 4
     assert attn.bwd_workspace_bytes(1, 1, 1, 96) == 0
     assert attn.bwd_workspace_bytes(0, 1, 128, 64) == 0
+
+
+def test_window_host_validation(lib):
+    from exact_attention_61_gb300 import attn
+    args = dict(q=A, k=2 * A * 64, v=3 * A * 64, o=4 * A * 64, lse=5 * A * 64, B=1, H=2, Nq=128, Nk=500,
+                d=64, window_left=64, window_right=0, kv_lens=None, align=1, scale=0.125, dtype=1,
+                workspace=None, workspace_bytes=0, stream=None)
+    for checked in (False, True):
+        f = lambda **kw: attn.attn_fwd_window(**{**args, **kw}, checked=checked)
+        assert f(align=2) == 1
+        assert f(align=-1) == 1
+        assert f(kv_lens=6 * A * 64 + 2) == 3
+        assert f(q=0) == 1
+        assert f(d=80) == 2
+        G = 1 << 40  # fake addresses far enough apart for 2^30 keys
+        assert f(Nk=1 << 30, q=G, k=2 * G, v=3 * G, o=4 * G, lse=5 * G) == 2  # Nq + Nk beyond 2^30
+        assert f(dtype=9) == 1
