@@ -104,6 +104,8 @@ def load(path: str = LIB_PATH):
             lib.attn_probe_tile.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64, ctypes.c_int,
                                                                     ctypes.c_void_p]
             lib.attn_probe_tile.restype = ctypes.c_int
+            lib.attn_probe_wait_timeout.argtypes = [ctypes.c_void_p]
+            lib.attn_probe_wait_timeout.restype = ctypes.c_int
             _lib = lib
     return _lib
 

@@ -131,6 +131,58 @@ cudaError_t launch_probe(const CUtensorMap* m, const void* p, float* s, float* o
 
 using namespace attn_sm103;
 
+namespace attn_sm103 {
+namespace {
+
+// Two warps wait, through the kernels' own bounded wait, on mbarriers that nothing ever
+// completes: warp 0 gives up when its time limit runs out and records the timeout; warp 1
+// sees the CTA's abort flag and gives up without recording. Shared memory only.
+__global__ void __launch_bounds__(64, 1) probe_wait_timeout_kernel(uint32_t* err) {
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ uint32_t abort_flag;
+    const uint32_t warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bars[0]), 1);
+        mbar_init(smem_addr(&bars[1]), 1);
+        abort_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    WaitCtx wc{err, &abort_flag, blockIdx.x};
+    const uint32_t where = 9000u + warp;  // role 9 (this probe), barrier = warp
+    if (warp == 1) {  // start half a second later, so that warp 0's limit runs out first
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 500ull * 1000ull * 1000ull) {
+        }
+    }
+    wait_warp(smem_addr(&bars[warp]), 0, wc, where, 7u + warp, true);
+    __syncthreads();
+}
+
+}  // namespace
+}  // namespace attn_sm103
+
+extern "C" int attn_probe_wait_timeout(void* stream) {
+    using namespace attn_sm103;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t* status = status_ptr(dev, &e);
+    if (!status) return cuda_fail(e);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(status, 0, 16, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    probe_wait_timeout_kernel<<<1, 64, 0, st>>>(status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t host[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(host, status, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return host[0] ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
 extern "C" int attn_probe_tile(const void* q, const void* k, const void* v, const void* p, float* s_out,
                                float* o_out, int64_t d, int dtype, void* stream) {
     if (!q || !k || !v || !p || !s_out || !o_out) return ATTN_ERR_INVALID_ARG;

@@ -34,6 +34,20 @@ extern "C" {
 int attn_probe_tile(const void* q, const void* k, const void* v, const void* p, float* s_out,
                     float* o_out, int64_t d, int dtype, void* stream);
 
+/*
+ * attn_probe_wait_timeout -- failure-detection test hook. Launches one CTA whose two
+ * warps wait, through the same bounded mbarrier wait the attention kernels use, on
+ * barriers that nothing ever completes: the first gives up after the kernels' wait
+ * limit (1.5 s) and records {code 1, block 0, 9000, 7} in the device status record;
+ * the second starts half a second later, sees the CTA's abort flag and gives up
+ * without recording. No fault, trap
+ * or hang is involved and the context stays usable. Synchronous on `stream` (current
+ * device). Returns ATTN_ERR_TIMEOUT when the timeout was recorded (the expected
+ * outcome), ATTN_OK if not, ATTN_ERR_CUDA on a CUDA error. The pages have no
+ * counterpart; it exists to test the timeout path on a GPU.
+ */
+int attn_probe_wait_timeout(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,3 +25,30 @@ def test_probe_tile_products(cuda_lib, d, dtype):
     # products of 16-bit values are exact in fp32; only the fp32 accumulation rounds
     assert s_err <= 1e-4 * max(1.0, np.abs(s_ref).max()), f"S = QK^T max err {s_err}"
     assert o_err <= 1e-4 * max(1.0, np.abs(o_ref).max()), f"O = PV max err {o_err}"
+
+
+@pytest.mark.gpu
+def test_bounded_wait_times_out_and_the_context_survives(cuda_lib):
+    """A wait that nothing completes gives up after the kernels' limit, records where,
+    and the other warp stops on the abort flag; a forward afterwards still works."""
+    import math
+    import time
+
+    import numpy as np
+    import torch
+
+    import oracle
+    from gen import make_qkv
+
+    t0 = time.perf_counter()
+    st = cuda_lib.load().attn_probe_wait_timeout(None)
+    dt = time.perf_counter() - t0
+    assert st == cuda_lib.ATTN_ERR_TIMEOUT
+    assert 1.0 < dt < 10.0
+    code, block, where, it = cuda_lib.device_error_info()
+    assert (code, block, where, it) == (1, 0, 9000, 7)
+    q, k, v = make_qkv(1, 2, 200, 64, "fp16", seed=99)
+    o, lse = cuda_lib.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, checked=True)
+    o_ref, _ = oracle.attn_fwd(q, k, v, True, 1.0 / math.sqrt(64))
+    assert np.abs(o.double().cpu().numpy() - o_ref).max() <= 4e-3
+    assert torch.cuda.synchronize() is None
