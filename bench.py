@@ -519,7 +519,7 @@ def bwd_flops(B_: int, H_: int, N_: int, d: int, causal: bool) -> float:
 
 def run_bwd(args) -> int:
     """--bwd: one backward pass (prep + main kernel + dQ cast) per timed step on the
-    headline problem, non-causal then causal, reported as TFLOP/s against the
+    headline problem (or --bwd-shape), non-causal then causal, reported as TFLOP/s against the
     measured bf16 peak. Single GPU; an extra measurement beside the headline line."""
     import torch
 
@@ -528,6 +528,7 @@ def run_bwd(args) -> int:
 
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA device")
+    B, H, N, D = (int(x) for x in args.bwd_shape.split(","))
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     attn.load()
@@ -581,10 +582,10 @@ def run_bwd(args) -> int:
     peaks = measured_peaks()
     ach = tflops(f_nc, ms_nc)
     out = {
-        "metric": "attention bwd TFLOP/s at B=4,H=16,N=4096,d=64 bf16", "value": tflops(f_nc + f_c, ms_nc + ms_c),
+        "metric": f"attention bwd TFLOP/s at B={B},H={H},N={N},d={D} bf16", "value": tflops(f_nc + f_c, ms_nc + ms_c),
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": n_warm,
         "ms_per_step": ms_nc + ms_c, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "b4h16n4096d64 bf16 backward, non-causal + causal per step", "B": B, "H": H,
+        "config": {"workload": f"b{B}h{H}n{N}d{D} bf16 backward, non-causal + causal per step", "B": B, "H": H,
                    "N": N, "d": D, "scale": scale, "seed": SEED,
                    "flops": "10 B H N^2 d (five N x N x d products), halved for causal",
                    "l2": "flushed before every step (write of 2x L2 size, outside the events)"},
@@ -624,6 +625,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward pass instead (extra measurement, 1 GPU)")
+    ap.add_argument("--bwd-shape", default="4,16,4096,64", metavar="B,H,N,d",
+                    help="problem of --bwd (default: the headline problem)")
     ap.add_argument("--decode", default=None, metavar="NAME",
                     help="time a KV-cache decode workload instead (extra measurement, 1 GPU)")
     return ap.parse_args(argv)

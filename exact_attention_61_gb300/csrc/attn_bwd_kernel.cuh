@@ -26,9 +26,9 @@
 //  - two warpgroups, one thread per key row (= TMEM lane) and half of the 128
 //    query columns each, turn S^T and dP^T into P^T and dS^T with exp2 and the
 //    LSE folded in log2 units, and write dS for the dQ product to shared memory;
-//  - a third warpgroup adds each dQ tile into an fp32 workspace with vector
-//    atomics (dQ gathers over key tiles owned by other CTAs), off the critical
-//    path of the other two;
+//  - a third warpgroup adds each dQ tile into an fp32 workspace (dQ gathers over key
+//    tiles owned by other CTAs) by staging it in shared memory and a TMA bulk
+//    reduce-add, off the critical path of the other two;
 //  - dK and dV stay in TMEM for the whole loop and are stored once at the end;
 //  - every mbarrier wait is bounded, as in the forward kernel.
 #pragma once
@@ -156,12 +156,15 @@ struct BwdCfg {
     static constexpr int kOffDS = kOffV + kTileBytes;   // dS: 128 keys x 128 queries, MN-major
     static constexpr int kOffStage = kOffDS + 128 * 128 * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;  // Q, then dO
-    // d = 64: the dQ tile is staged (fp32, 2 boxes of 32 columns x 128 rows, 128-byte
-    // swizzle) and added to the accumulator by TMA; d = 128 has no room and uses atomics.
-    static constexpr bool kTmaDq = D == 64;
-    static constexpr int kOffDqStage = kOffStage + kStages * kStageBytes;
+    // The fp32 dQ tile is staged in shared memory (boxes of 32 columns x 128 rows,
+    // 128-byte swizzle) and added to the accumulator by TMA. d = 64 has a stage of its
+    // own; at d = 128 there is no room, and the tile (64 KB) is staged in the Q/dO ring
+    // stage of its own iteration, which every MMA of that iteration has finished reading
+    // once dQ is done; the stage returns to the loader only after the reduce read it.
+    static constexpr bool kDqInRing = D == 128;
     static constexpr int kDqBoxBytes = 128 * 32 * 4;
-    static constexpr int kOffVec = kOffDqStage + (kTmaDq ? 2 * kDqBoxBytes : 0);
+    static constexpr int kOffDqStage = kOffStage + kStages * kStageBytes;
+    static constexpr int kOffVec = kOffDqStage + (kDqInRing ? 0 : (D / 32) * kDqBoxBytes);
     static constexpr int kVecBytes = 2 * 128 * 4;       // lse2[128], D[128] per stage
     static constexpr int kOffBar = kOffVec + kStages * kVecBytes;
     static constexpr int kBarKV = 0;
@@ -224,7 +227,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages) count = 1 + 8;  // MMA + compute warps
+            if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages)
+                count = 1 + 8 + (C::kDqInRing ? 1 : 0);  // MMA + compute warps (+ dQ store)
             if (i == C::kBarPds) count = 8;                                              // compute warps
             if (i == C::kBarDqRead) count = 4;                                           // dQ warps
             mbar_init(bar(i), count);
@@ -358,63 +362,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t r = wq * 32u + lane;
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
         const bool leader = warp == C::kWarpDq && lane == 0;
-        if (C::kTmaDq && leader) tma_prefetch_desc(&tmDQ);
+        if (leader) tma_prefetch_desc(&tmDQ);
         for (int it = 0; it < n_it; ++it) {
             if (!wait_warp(bar(C::kBarDqFull), it & 1, wc, kRoleBwdDq * 1000 + C::kBarDqFull, it)) break;
             tc_fence_after_sync();
             const int q0 = (qt0 + it) * 128;
-            const int qrow = q0 + static_cast<int>(r);
-            if constexpr (C::kTmaDq) {
-                uint32_t o[2][32];
-                tmem_ld32(lane_base + C::colDQ, o[0]);
-                tmem_ld32(lane_base + C::colDQ + 32, o[1]);
+            const int s = it % C::kStages;
+            const uint32_t stage = C::kDqInRing ? sQ(s) : base + C::kOffDqStage;
+            // The previous tile's reduce has finished reading a stage of its own.
+            if (!C::kDqInRing && leader) tma_store_wait_read_all();
+            if (!C::kDqInRing) named_bar_sync(1, 128);
+#pragma unroll 1
+            for (int b = 0; b < D / 32; ++b) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + C::colDQ + 32 * b, o);
                 tmem_ld_wait();
-                reg_fence(o[0]);
-                reg_fence(o[1]);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::kBarDqRead));  // the dQ columns are free
-                // The previous tile's reduce has finished reading the stage.
-                if (leader) tma_store_wait_read_all();
-                named_bar_sync(1, 128);
+                reg_fence(o);
+                const uint32_t row = stage + b * C::kDqBoxBytes + r * 128u;
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const uint32_t row = base + C::kOffDqStage + b * C::kDqBoxBytes + r * 128u;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        st_shared_v4(row + ((ch ^ (r & 7u)) << 4), o[b][4 * ch], o[b][4 * ch + 1], o[b][4 * ch + 2],
-                                     o[b][4 * ch + 3]);
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (leader && *wc.abort == 0u) {
-                    tma_reduce_add_3d(&tmDQ, base + C::kOffDqStage, 0, q0, bh);
-                    tma_reduce_add_3d(&tmDQ, base + C::kOffDqStage + C::kDqBoxBytes, 32, q0, bh);
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_v4(row + ((ch ^ (r & 7u)) << 4), o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarDqRead));  // the dQ columns are free
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (leader) {
+                if (*wc.abort == 0u) {
+#pragma unroll 1
+                    for (int b = 0; b < D / 32; ++b)
+                        tma_reduce_add_3d(&tmDQ, stage + b * C::kDqBoxBytes, 32 * b, q0, bh);
                     tma_store_commit();
                 }
-            } else {
-                float* dst = p.dq_acc + (static_cast<size_t>(bh) * N + qrow) * D;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_base + C::colDQ + 32 * c, o);
-                    tmem_ld_wait();
-                    reg_fence(o);
-                    if (qrow < N) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + e),
-                                      make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                                  __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3])));
-                    }
+                // In the ring, the stage goes back to the loader once the reduce read it.
+                if (C::kDqInRing) {
+                    tma_store_wait_read_all();
+                    mbar_arrive(bar(C::kBarQdEmpty + s));
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::kBarDqRead));
             }
         }
         // Every reduce is complete in global memory before the CTA exits.
-        if (C::kTmaDq && leader) tma_store_wait_all();
+        if (leader) tma_store_wait_all();
     } else {
         // ================================ compute warpgroups ==========================
         // Warpgroup h handles query columns [64h, 64h + 64) of S^T and dP^T.
