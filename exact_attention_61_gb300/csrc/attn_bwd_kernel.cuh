@@ -156,15 +156,14 @@ struct BwdCfg {
     static constexpr int kOffDS = kOffV + kTileBytes;   // dS: 128 keys x 128 queries, MN-major
     static constexpr int kOffStage = kOffDS + 128 * 128 * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;  // Q, then dO
-    // The fp32 dQ tile is staged in shared memory (boxes of 32 columns x 128 rows,
-    // 128-byte swizzle) and added to the accumulator by TMA. d = 64 has a stage of its
-    // own; at d = 128 there is no room, and the tile (64 KB) is staged in the Q/dO ring
-    // stage of its own iteration, which every MMA of that iteration has finished reading
-    // once dQ is done; the stage returns to the loader only after the reduce read it.
-    static constexpr bool kDqInRing = D == 128;
+    // The fp32 dQ tile (128 rows x d, exactly one Q/dO ring stage) is staged in the ring
+    // stage of its own iteration, in boxes of 32 columns x 128 rows with the 128-byte
+    // swizzle, and added to the accumulator by TMA. Every MMA of the iteration has
+    // finished reading the stage once dQ is done; the stage returns to the loader only
+    // after the reduce has read it.
     static constexpr int kDqBoxBytes = 128 * 32 * 4;
-    static constexpr int kOffDqStage = kOffStage + kStages * kStageBytes;
-    static constexpr int kOffVec = kOffDqStage + (kDqInRing ? 0 : (D / 32) * kDqBoxBytes);
+    static_assert((D / 32) * kDqBoxBytes == kStageBytes, "dQ tile = one ring stage");
+    static constexpr int kOffVec = kOffStage + kStages * kStageBytes;
     static constexpr int kVecBytes = 2 * 128 * 4;       // lse2[128], D[128] per stage
     static constexpr int kOffBar = kOffVec + kStages * kVecBytes;
     static constexpr int kBarKV = 0;
@@ -228,7 +227,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
             if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages)
-                count = 1 + 8 + (C::kDqInRing ? 1 : 0);  // MMA + compute warps (+ dQ store)
+                count = 1 + 8 + 1;  // MMA, compute warps, dQ store
             if (i == C::kBarPds) count = 8;                                              // compute warps
             if (i == C::kBarDqRead) count = 4;                                           // dQ warps
             mbar_init(bar(i), count);
@@ -356,8 +355,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     } else if (warp >= C::kWarpDq) {
         // ================================ dQ read-out ==================================
         // TMEM lane r of the dQ tile is query q0 + r; the tile is added to the fp32
-        // accumulator (other CTAs add the other key tiles' parts): at d = 64 through a
-        // swizzled shared-memory stage and TMA reduce-add, at d = 128 with vector atomics.
+        // accumulator (other CTAs add the other key tiles' parts) through the swizzled
+        // ring stage of its iteration and a TMA bulk reduce-add.
         const uint32_t wq = warp - C::kWarpDq;
         const uint32_t r = wq * 32u + lane;
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
@@ -368,10 +367,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             tc_fence_after_sync();
             const int q0 = (qt0 + it) * 128;
             const int s = it % C::kStages;
-            const uint32_t stage = C::kDqInRing ? sQ(s) : base + C::kOffDqStage;
-            // The previous tile's reduce has finished reading a stage of its own.
-            if (!C::kDqInRing && leader) tma_store_wait_read_all();
-            if (!C::kDqInRing) named_bar_sync(1, 128);
+            const uint32_t stage = sQ(s);
 #pragma unroll 1
             for (int b = 0; b < D / 32; ++b) {
                 uint32_t o[32];
@@ -395,11 +391,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         tma_reduce_add_3d(&tmDQ, stage + b * C::kDqBoxBytes, 32 * b, q0, bh);
                     tma_store_commit();
                 }
-                // In the ring, the stage goes back to the loader once the reduce read it.
-                if (C::kDqInRing) {
-                    tma_store_wait_read_all();
-                    mbar_arrive(bar(C::kBarQdEmpty + s));
-                }
+                // The stage goes back to the loader once the reduce has read it.
+                tma_store_wait_read_all();
+                mbar_arrive(bar(C::kBarQdEmpty + s));
             }
         }
         // Every reduce is complete in global memory before the CTA exits.
