@@ -13,8 +13,8 @@ namespace attn_sm103 {
 constexpr int kBwdTile = 128;
 
 struct BwdParams {
-    const float* lse2;  // [BH][Npad] LSE * log2(e); +inf on padded rows (P = 0 there)
-    const float* dvec;  // [BH][Npad] D = rowsum(dO * O); 0 on padded rows
+    const float* lse2;  // [BH][Npad] -LSE * log2(e); -inf on padded rows (P = 0 there)
+    const float* dvec;  // [BH][Npad] -D = -rowsum(dO * O); 0 on padded rows
     float* dq_acc;      // [BH][N][d] fp32 sum of dS K over the key tiles (unscaled)
     void* dk;           // [BH][N][d] dtype
     void* dv;           // [BH][N][d] dtype

@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int j = j0 + static_cast<int>(r);      // this thread's key
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
         const float qk = p.qk_scale;
+        const float2 qk2 = make_float2(qk, qk);
         const uint32_t sDS = base + C::kOffDS + h * C::kBoxBytes + r * 128u;
         bool ok = true;
         for (int it = 0; it < n_it && ok; ++it) {
@@ -422,10 +423,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             // iteration (issued before them) has finished reading the dS tile.
             tc_fence_after_sync();
             const float* vec = reinterpret_cast<const float*>(smem_bwd + C::kOffVec + s * C::kVecBytes);
-            const float* lse2 = vec + 64 * h;
-            const float* dvec = vec + 128 + 64 * h;
+            const float* nlse2 = vec + 64 * h;        // -LSE log2(e) of this half's query rows
+            const float* ndvec = vec + 128 + 64 * h;  // -D
             const bool diag = CAUSAL && q0 == j0;  // only this Q tile has keys after queries
             const bool key_out = j >= N;           // padded key row: P = 0
+            // causal: on the diagonal tile key r sees query columns >= r only
+            const bool mask_tile = key_out || diag;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 const uint32_t col32 = 64u * h + 32u * c;  // first fp32 column of this chunk
@@ -437,17 +440,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 reg_fence(dr);
                 uint32_t pk[16], dk[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int col = 32 * c + e;                     // within this half
-                    const int qcol = 64 * static_cast<int>(h) + col;  // within the Q tile
-                    float p0 = ex2_ftz(fmaf(__uint_as_float(sr[e]), qk, -lse2[col]));
-                    float p1 = ex2_ftz(fmaf(__uint_as_float(sr[e + 1]), qk, -lse2[col + 1]));
-                    if (key_out || (diag && static_cast<int>(r) > qcol)) p0 = 0.f;
-                    if (key_out || (diag && static_cast<int>(r) > qcol + 1)) p1 = 0.f;
-                    const float ds0 = p0 * (__uint_as_float(dr[e]) - dvec[col]);
-                    const float ds1 = p1 * (__uint_as_float(dr[e + 1]) - dvec[col + 1]);
-                    pk[e >> 1] = pack2<BF16>(p0, p1);
-                    dk[e >> 1] = pack2<BF16>(ds0, ds1);
+                for (int e = 0; e < 32; e += 4) {
+                    const int col = 32 * c + e;  // within this half
+                    // -LSE log2(e) and -D of four query rows (the prologue stores them negated)
+                    const float4 nl = *reinterpret_cast<const float4*>(nlse2 + col);
+                    const float4 nd = *reinterpret_cast<const float4*>(ndvec + col);
+                    const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), qk2,
+                                                 make_float2(nl.x, nl.y));
+                    const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])),
+                                                 qk2, make_float2(nl.z, nl.w));
+                    float pe[4] = {ex2_ftz(y0.x), ex2_ftz(y0.y), ex2_ftz(y1.x), ex2_ftz(y1.y)};
+                    if (mask_tile) {
+                        const int qcol = 64 * static_cast<int>(h) + col;  // within the Q tile
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            if (key_out || static_cast<int>(r) > qcol + k) pe[k] = 0.f;
+                    }
+                    const float2 p0 = make_float2(pe[0], pe[1]), p1 = make_float2(pe[2], pe[3]);
+                    const float2 ds0 = __fmul2_rn(
+                        p0, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                       make_float2(nd.x, nd.y)));
+                    const float2 ds1 = __fmul2_rn(
+                        p1, __fadd2_rn(make_float2(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                       make_float2(nd.z, nd.w)));
+                    pk[e >> 1] = pack2<BF16>(p0.x, p0.y);
+                    pk[(e >> 1) + 1] = pack2<BF16>(p1.x, p1.y);
+                    dk[e >> 1] = pack2<BF16>(ds0.x, ds0.y);
+                    dk[(e >> 1) + 1] = pack2<BF16>(ds1.x, ds1.y);
                 }
                 // 16-bit P^T / dS^T packed in place: half h lives in columns
                 // [64h, 64h + 32), chunk c in its 16 columns (already read above).
@@ -509,8 +528,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
 }
 
-// D_i = rowsum(dO * O), lse2_i = LSE_i log2(e) (+inf where LSE = -inf or i >= N, so that
-// P = 0 there), and the zeroed dQ accumulator. One warp per row of [BH][Npad].
+// -D_i = -rowsum(dO * O), -lse2_i = -LSE_i log2(e) (-inf where LSE = -inf or i >= N, so
+// that P = 0 there), and the zeroed dQ accumulator. One warp per row of [BH][Npad]. The
+// main kernel adds them, so they are stored negated.
 template <bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams p) {
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -520,8 +540,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams 
     const size_t vrow = static_cast<size_t>(bh) * p.Npad + i;
     if (i >= p.N) {
         if (lane == 0) {
-            p.lse2[vrow] = INFINITY;
-            p.dvec[vrow] = 0.f;
+            p.lse2[vrow] = -INFINITY;
+            p.dvec[vrow] = -0.f;
         }
         return;
     }
@@ -544,8 +564,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams 
     for (int w = 16; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
     if (lane == 0) {
         const float l = p.lse[static_cast<size_t>(bh) * p.N + i];
-        p.lse2[vrow] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
-        p.dvec[vrow] = acc;
+        p.lse2[vrow] = l == -INFINITY ? -INFINITY : -(l * 1.4426950408889634f);
+        p.dvec[vrow] = -acc;
     }
 }
 
