@@ -141,6 +141,30 @@ def test_headline_size_sampled_heads(cuda_lib, causal):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_d128_large_sampled_heads(cuda_lib, causal):
+    """B=2, H=8, N=3000 (ragged), d=128, fp16: the whole problem on the GPU, two heads
+    checked element by element (the d=128 dQ path stages in the Q/dO ring)."""
+    B, H, N, d, dtype = 2, 8, 3000, 128, "fp16"
+    q, k, v, do = _inputs(B, H, N, d, dtype, seed=62700 + int(causal))
+    scale = 1.0 / math.sqrt(d)
+    gq, gk, gv, gdo = (t.cuda() for t in (q, k, v, do))
+    o, lse = cuda_lib.fwd(gq, gk, gv, causal=causal, scale=scale, checked=True)
+    got = _run(cuda_lib, gq, gk, gv, gdo, o, lse, causal, scale)
+    for b, h in ((0, 3), (1, 7)):
+        sl = lambda t: t[b:b + 1, h:h + 1].contiguous()
+        qs, ks, vs, dos = (sl(t) for t in (q, k, v, do))
+        o_ref, _ = oracle.attn_fwd(qs, ks, vs, causal, scale)
+        dq, dk, dv = oracle.attn_bwd(qs, ks, vs, dos, causal, scale)
+        m = oracle.attn_bwd_materialised(qs, ks, vs, dos, causal, scale)
+        dD = _d_error(oracle.to_f64(dos), sl(o).to(torch.float64).cpu().numpy(), o_ref, U[dtype])
+        g = {key: sl(t) for key, t in got.items()}
+        _check(f"d128 b{b}h{h}{'c' if causal else ''}", g, {"dq": dq, "dk": dk, "dv": dv}, m,
+               oracle.to_f64(qs), oracle.to_f64(ks), oracle.to_f64(dos), dD, scale, dtype, N)
+        del m
+
+
+@pytest.mark.gpu
 def test_dk_dv_deterministic_and_dq_reproducible(cuda_lib):
     q, k, v, do = (t.cuda() for t in _inputs(2, 4, 1500, 64, "bf16", seed=62500))
     o, lse = cuda_lib.fwd(q, k, v, causal=True, checked=True)
