@@ -605,6 +605,60 @@ def run_bwd(args) -> int:
     return 0
 
 
+def run_fwd_shapes(args) -> int:
+    """--fwd-shapes "B,H,N,d;...": the forward (non-causal, causal) on other problem
+    sizes, one JSON line each, L2 flushed between launches. An extra measurement
+    beside the headline line (the sequence sweep and the wide-head long problem)."""
+    import torch
+
+    from exact_attention_61_gb300 import attn, counts
+    from gen import make_qkv
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    attn.load()
+    peaks = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for spec in args.fwd_shapes.split(";"):
+        b_, h_, n_, d_ = (int(x) for x in spec.split(","))
+        q, k, v = (t.to(dev) for t in make_qkv(b_, h_, n_, d_, DTYPE, SEED))
+        o = torch.empty_like(q)
+        lse = torch.empty((b_, h_, n_), dtype=torch.float32, device=dev)
+        scale = 1.0 / math.sqrt(d_)
+        res = {}
+        for causal in (False, True):
+            def launch():
+                st = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   b_, h_, n_, d_, causal, scale, attn.ATTN_BF16, stream.cuda_stream)
+                if st != attn.ATTN_OK:
+                    raise RuntimeError(f"attn_fwd failed: {attn.strerror(st)}")
+            for i in range(max(args.warmup, 3)):
+                flush.fill_(i & 0xFF)
+                launch()
+            ts = []
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+                ts.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            ms = statistics.fmean(a.elapsed_time(b) for a, b in ts)
+            f = counts.attn_flops(b_, h_, n_, d_, causal)
+            res["causal" if causal else "noncausal"] = {"ms_mean": ms, "tflops": tflops(f, ms),
+                                                        "frac_of_peak": tflops(f, ms) / peaks["bf16_tflops"]}
+        print(json.dumps({"metric": f"attention fwd TFLOP/s at B={b_},H={h_},N={n_},d={d_} bf16",
+                          "unit": "TFLOP/s", "steps": args.steps, "dtype": "bf16", "data": "synthetic",
+                          "l2": "flushed before every launch", **res}), flush=True)
+        del q, k, v, o, lse
+    return 0
+
+
 def _pct(xs, p):
     s = sorted(xs)
     return s[min(len(s) - 1, max(0, int(round(p / 100.0 * (len(s) - 1)))))]
@@ -627,6 +681,8 @@ def parse_args(argv=None):
                     help="time the backward pass instead (extra measurement, 1 GPU)")
     ap.add_argument("--bwd-shape", default="4,16,4096,64", metavar="B,H,N,d",
                     help="problem of --bwd (default: the headline problem)")
+    ap.add_argument("--fwd-shapes", default=None, metavar="B,H,N,d;...",
+                    help="time the forward on other sizes instead (extra measurement, 1 GPU)")
     ap.add_argument("--decode", default=None, metavar="NAME",
                     help="time a KV-cache decode workload instead (extra measurement, 1 GPU)")
     return ap.parse_args(argv)
@@ -642,6 +698,8 @@ def main(argv=None) -> int:
         return run_decode(args)
     if args.bwd:
         return run_bwd(args)
+    if args.fwd_shapes:
+        return run_fwd_shapes(args)
     return run_ours(args)
 
 
