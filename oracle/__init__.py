@@ -89,6 +89,9 @@ def _load():
                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                             ctypes.c_double]
             lib.oracle_attn_bwd.restype = ctypes.c_int
+            lib.oracle_attn_bwd_window.argtypes = [_DP] * 7 + [ctypes.c_int64] * 7 + [
+                _I64P, ctypes.c_int, ctypes.c_double]
+            lib.oracle_attn_bwd_window.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -354,3 +357,26 @@ def window_mask(B, Nq, Nk, left=-1, right=-1, kv_lens=None, align="top_left"):
     if right >= 0:
         keep = keep & (j <= diag + right)
     return keep
+
+
+def attn_bwd_window(q, k, v, dout, left: int = -1, right: int = -1, kv_lens=None,
+                    align: str = "top_left", scale: float | None = None):
+    """Gradients (dQ [B,H,Nq,d], dK, dV [B,H,Nk,d]) of sum(dO * O) for O of
+    :func:`attn_fwd_window` (C, fp64): each query row over exactly the keys it sees."""
+    q64, k64, v64, g64 = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    B, H, Nq, d = q64.shape
+    Nk = k64.shape[2]
+    if k64.shape != (B, H, Nk, d) or v64.shape != k64.shape or g64.shape != q64.shape:
+        raise ValueError("q, dout [B,H,Nq,d] and k, v [B,H,Nk,d] must agree")
+    scale = default_scale(d) if scale is None else float(scale)
+    lens = None
+    if kv_lens is not None:
+        lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int64).reshape(B))
+    dq, dk, dv = np.empty_like(q64), np.empty_like(k64), np.empty_like(k64)
+    rc = _load().oracle_attn_bwd_window(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64), _ptr(dq), _ptr(dk),
+                                        _ptr(dv), B, H, Nq, Nk, d, int(left), int(right),
+                                        lens.ctypes.data_as(_I64P) if lens is not None else None,
+                                        {"top_left": 0, "bottom_right": 1}[align], scale)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd_window failed with code {rc}")
+    return dq, dk, dv

@@ -353,6 +353,88 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
     return failed ? -2 : 0;
 }
 
+/* Backward of oracle_attn_fwd_window: the gradients of sum(dO * O) for Nq query rows
+ * against Nk keys with key padding and a sliding window, each row over exactly the
+ * keys the forward lets it see (same readings as oracle_attn_fwd_window), with the
+ * chain rule of oracle_attn_bwd. q, dout, dq: [BH][Nq][d]; k, v, dk, dv: [BH][Nk][d].
+ * Rows that see no key have dQ = 0 and add nothing to dK, dV; padded keys get
+ * dK = dV = 0. One head per OpenMP task, rows in order. */
+int oracle_attn_bwd_window(const double* q, const double* k, const double* v, const double* dout,
+                           double* dq, double* dk, double* dv, int64_t B, int64_t H, int64_t Nq,
+                           int64_t Nk, int64_t d, int64_t left, int64_t right,
+                           const int64_t* kv_lens, int align, double scale)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1)
+        return -1;
+    if (!(scale > 0.0) || !isfinite(scale)) return -1;
+    if (kv_lens)
+        for (int64_t b = 0; b < B; ++b)
+            if (kv_lens[b] < 0 || kv_lens[b] > Nk) return -1;
+    int failed = 0;
+#pragma omp parallel reduction(| : failed)
+    {
+        double* p = (double*)malloc((size_t)Nk * sizeof(double));
+        double* dp = (double*)malloc((size_t)Nk * sizeof(double));
+        if (!p || !dp) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bh = 0; bh < B * H; ++bh) {
+                const double* Q = q + bh * Nq * d;
+                const double* K = k + bh * Nk * d;
+                const double* V = v + bh * Nk * d;
+                const double* DO = dout + bh * Nq * d;
+                double* DQ = dq + bh * Nq * d;
+                double* DK = dk + bh * Nk * d;
+                double* DV = dv + bh * Nk * d;
+                memset(DK, 0, (size_t)(Nk * d) * sizeof(double));
+                memset(DV, 0, (size_t)(Nk * d) * sizeof(double));
+                const int64_t n_b = kv_lens ? kv_lens[bh / H] : Nk;
+                for (int64_t i = 0; i < Nq; ++i) {
+                    const int64_t diag = i + (align ? n_b - Nq : 0);
+                    int64_t lo = left < 0 ? 0 : diag - left;
+                    int64_t hi = right < 0 ? n_b - 1 : diag + right;
+                    if (lo < 0) lo = 0;
+                    if (hi > n_b - 1) hi = n_b - 1;
+                    const double* qi = Q + i * d;
+                    const double* doi = DO + i * d;
+                    for (int64_t t = 0; t < d; ++t) DQ[i * d + t] = 0.0;
+                    if (hi < lo) continue;
+                    double m = -INFINITY;
+                    for (int64_t j = lo; j <= hi; ++j) {
+                        double dot = 0.0;
+                        for (int64_t t = 0; t < d; ++t) dot += qi[t] * K[j * d + t];
+                        p[j] = scale * dot;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double l = 0.0;
+                    for (int64_t j = lo; j <= hi; ++j) l += exp(p[j] - m);
+                    const double lse = m + log(l);
+                    double Di = 0.0;
+                    for (int64_t j = lo; j <= hi; ++j) {
+                        p[j] = exp(p[j] - lse);
+                        double dot = 0.0;
+                        for (int64_t t = 0; t < d; ++t) dot += doi[t] * V[j * d + t];
+                        dp[j] = dot;
+                        Di += p[j] * dot;
+                    }
+                    for (int64_t j = lo; j <= hi; ++j) {
+                        const double ds = p[j] * (dp[j] - Di);
+                        for (int64_t t = 0; t < d; ++t) {
+                            DV[j * d + t] += p[j] * doi[t];
+                            DQ[i * d + t] += scale * ds * K[j * d + t];
+                            DK[j * d + t] += scale * ds * qi[t];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return failed ? -2 : 0;
+}
+
 /* Threads an OpenMP parallel region of this library uses. */
 int oracle_num_threads(void)
 {

@@ -147,3 +147,69 @@ def test_planted_mistakes_are_caught(kind):
     assert caught_autograd
     if kind in ("D_sign", "no_D"):  # the sum rule alone catches a wrong D term
         assert caught_sums
+
+
+# ---- windows, padding and Nq != Nk ------------------------------------------------------
+
+def _torch_grads_mask(q, k, v, do, keep, scale):
+    """torch float64 autograd through an explicit forward with a boolean [B,1|H,Nq,Nk]
+    mask; rows without keys are given O = 0 (no gradient) as the oracle defines."""
+    q, k, v = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    s = scale * q @ k.transpose(-1, -2)
+    keep_t = torch.tensor(keep)
+    s = s.masked_fill(~keep_t, float("-inf"))
+    any_key = keep_t.any(-1, keepdim=True)
+    p = torch.softmax(torch.where(any_key, s, torch.zeros_like(s)), dim=-1) * any_key
+    o = p @ v
+    (o * torch.tensor(do)).sum().backward()
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+@pytest.mark.parametrize("Nq,Nk,left,right,lens,align", [
+    (9, 9, -1, -1, None, "top_left"),
+    (9, 9, 3, 0, None, "top_left"),
+    (5, 17, 4, 0, [17, 9], "bottom_right"),
+    (12, 7, -1, 0, [7, 3], "bottom_right"),
+    (8, 20, 2, 2, [20, 0], "top_left"),
+    (6, 6, 0, 0, None, "top_left"),
+])
+def test_window_backward_matches_torch_autograd(Nq, Nk, left, right, lens, align):
+    B, H, d = 2, 2, 4
+    g = np.random.default_rng(Nq * 100 + Nk + left)
+    q, do = g.standard_normal((B, H, Nq, d)), g.standard_normal((B, H, Nq, d))
+    k, v = g.standard_normal((B, H, Nk, d)), g.standard_normal((B, H, Nk, d))
+    got = oracle.attn_bwd_window(q, k, v, do, left, right, lens, align, scale=0.6)
+    keep = oracle.window_mask(B, Nq, Nk, left, right, lens, align)[:, None]
+    want = _torch_grads_mask(q, k, v, do, keep, 0.6)
+    for a, w, name in zip(got, want, ("dq", "dk", "dv")):
+        np.testing.assert_allclose(a, w, rtol=0, atol=1e-11, err_msg=name)
+    if lens is not None:  # padded keys receive no gradient
+        for b, n in enumerate(lens):
+            assert np.all(got[1][b, :, n:] == 0) and np.all(got[2][b, :, n:] == 0)
+
+
+def test_window_backward_reduces_to_square_and_finite_differences():
+    q, k, v, do = _rand(1, 2, 10, 3, seed=31)
+    for causal in (False, True):
+        a = oracle.attn_bwd_window(q, k, v, do, -1, 0 if causal else -1, scale=0.8)
+        b = oracle.attn_bwd(q, k, v, do, causal, 0.8)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+    # a two-sided window on a tiny problem: central differences of the windowed forward
+    q, k, v, do = _rand(1, 1, 5, 3, seed=32)
+    grads = oracle.attn_bwd_window(q, k, v, do, 1, 1, scale=0.9)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attn_fwd_window(q_, k_, v_, 1, 1, scale=0.9)
+        return float((o * do).sum())
+
+    h = 1e-5
+    for which, gr in enumerate(grads):
+        for idx in np.ndindex(gr.shape):
+            x = [q, k, v]
+            plus = [a.copy() for a in x]
+            minus = [a.copy() for a in x]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fd = (loss(*plus) - loss(*minus)) / (2 * h)
+            assert abs(fd - gr[idx]) < 1e-8
