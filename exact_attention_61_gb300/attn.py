@@ -57,6 +57,11 @@ _BWD_ARGS = ([ctypes.c_void_p] * 9 + [ctypes.c_int64] * 4 +
               ctypes.c_void_p])
 
 
+_BWD_WIN_ARGS = ([ctypes.c_void_p] * 9 + [ctypes.c_int64] * 7 +
+                 [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                  ctypes.c_void_p])
+
+
 class AttnError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(msg)
@@ -93,6 +98,10 @@ def load(path: str = LIB_PATH):
             lib.attn_bwd.restype = ctypes.c_int
             lib.attn_bwd_checked.argtypes = _BWD_ARGS
             lib.attn_bwd_checked.restype = ctypes.c_int
+            lib.attn_bwd_window.argtypes = _BWD_WIN_ARGS
+            lib.attn_bwd_window.restype = ctypes.c_int
+            lib.attn_bwd_window_checked.argtypes = _BWD_WIN_ARGS
+            lib.attn_bwd_window_checked.restype = ctypes.c_int
             lib.attn_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 4
             lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_strerror.argtypes = [ctypes.c_int]
@@ -343,6 +352,39 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = No
                   scale, _dtype_code(q), workspace.data_ptr(), workspace.numel(), stream.cuda_stream,
                   checked=checked)
     _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def bwd_window(q, k, v, o, lse, dout, window=(-1, -1), kv_lens=None, align: str = "top_left",
+               scale: Optional[float] = None, workspace=None, stream=None, checked: bool = False):
+    """Gradients (dq [B,H,Nq,d], dk, dv [B,H,Nk,d]) of sum(dout * o) for
+    o, lse = fwd_window(q, k, v, window, kv_lens, align, scale)."""
+    import torch
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    for t, n in ((q, Nq), (o, Nq), (dout, Nq), (k, Nk), (v, Nk)):
+        if t.dim() != 4 or t.shape != (B, H, n, d) or t.dtype != q.dtype:
+            raise ValueError("q, o, dout [B,H,Nq,d] and k, v [B,H,Nk,d] of one dtype")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    if kv_lens is not None and (kv_lens.dtype != torch.int32 or kv_lens.shape != (B,) or not kv_lens.is_cuda):
+        raise ValueError("kv_lens must be a CUDA int32 tensor of shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+    if workspace is None:
+        workspace = torch.empty((max(bwd_workspace_bytes(B, H, Nq, d), 16),), dtype=torch.uint8,
+                                device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    fn = load().attn_bwd_window_checked if checked else load().attn_bwd_window
+    st = int(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, int(window[0]), int(window[1]),
+                kv_lens.data_ptr() if kv_lens is not None else None, ALIGN[align], float(scale), _dtype_code(q),
+                workspace.data_ptr(), workspace.numel(), stream.cuda_stream))
+    _check(st, "attn_bwd_window")
     return dq, dk, dv
 
 

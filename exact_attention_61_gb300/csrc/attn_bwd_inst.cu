@@ -1,4 +1,5 @@
-// One (head dimension, dtype) pair of backward-kernel instances, causal or not.
+// One (head dimension, dtype) pair of backward-kernel instances: causal or not, plain or
+// with padding / windows / Nq != Nk.
 // Compiled once per pair with -DATTN_INST_D=<64|128> -DATTN_INST_BF16=<0|1>.
 #include <atomic>
 
@@ -12,10 +13,10 @@
 namespace attn_sm103 {
 namespace {
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool EXT>
 cudaError_t launch_bwd_one(const CUtensorMap* m, const BwdParams& p, cudaStream_t s) {
     using C = BwdCfg<D>;
-    auto* kern = attn_bwd_kernel<D, CAUSAL, BF16>;
+    auto* kern = attn_bwd_kernel<D, CAUSAL, BF16, EXT>;
     // The dynamic shared-memory opt-in is per device; remember which devices have it.
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -27,7 +28,7 @@ cudaError_t launch_bwd_one(const CUtensorMap* m, const BwdParams& p, cudaStream_
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const unsigned grid = static_cast<unsigned>(p.n_tiles) * static_cast<unsigned>(p.BH);
+    const unsigned grid = static_cast<unsigned>(p.n_ktiles) * static_cast<unsigned>(p.BH);
     kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], p);
     return cudaGetLastError();
 }
@@ -43,10 +44,14 @@ cudaError_t launch_bwd_one(const CUtensorMap* m, const BwdParams& p, cudaStream_
 #endif
 #define ATTN_BWD_NAME ATTN_CAT(ATTN_CAT(ATTN_CAT(launch_bwd_d, ATTN_INST_D), _), ATTN_DT_SUFFIX)
 
-cudaError_t ATTN_BWD_NAME(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
+cudaError_t ATTN_BWD_NAME(bool causal, bool ext, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
     constexpr bool kBf16 = ATTN_INST_BF16 != 0;
-    return causal ? launch_bwd_one<ATTN_INST_D, true, kBf16>(maps, p, s)
-                  : launch_bwd_one<ATTN_INST_D, false, kBf16>(maps, p, s);
+    constexpr int kD = ATTN_INST_D;
+    if (ext)
+        return causal ? launch_bwd_one<kD, true, kBf16, true>(maps, p, s)
+                      : launch_bwd_one<kD, false, kBf16, true>(maps, p, s);
+    return causal ? launch_bwd_one<kD, true, kBf16, false>(maps, p, s)
+                  : launch_bwd_one<kD, false, kBf16, false>(maps, p, s);
 }
 
 }  // namespace attn_sm103

@@ -19,10 +19,18 @@ struct BwdParams {
     void* dk;           // [BH][N][d] dtype
     void* dv;           // [BH][N][d] dtype
     uint32_t* err;      // device status record {code, block, where, iteration}
-    int N;              // sequence length (queries = keys)
-    int Npad;           // N rounded up to a multiple of 128
+    int Nq;             // query rows per head
+    int Nk;             // keys per head
+    int Npad;           // Nq rounded up to a multiple of 128
     int BH;             // batch * heads
-    int n_tiles;        // Npad / 128
+    int H;              // heads (batch element of head bh is bh / H)
+    int n_ktiles;       // ceil(Nk / 128): CTAs per head
+    // Masks beyond the plain causal one (EXT kernels only; the same readings as the
+    // forward's): valid keys per batch element, diagonal alignment, window bounds.
+    const int32_t* kv_lens;  // [B] or null
+    int align_br;            // diagonal of row i: key i (0) or i + n_b - Nq (1)
+    int win_right;           // causal kernels: key j visible to row i iff j <= diag + win_right
+    int win_left;            // >= 0: j >= diag - win_left; < 0: unbounded
     float qk_scale;     // scale * log2(e)
     float scale;
 };
@@ -34,7 +42,7 @@ struct BwdPrepParams {
     float* lse2;        // [BH][Npad]
     float* dvec;        // [BH][Npad]
     float* dq_acc;      // [BH][N][d], zeroed here
-    int N, Npad, BH, d;
+    int N, Npad, BH, d;  // N: query rows
 };
 
 struct BwdConvertParams {
@@ -46,10 +54,14 @@ struct BwdConvertParams {
 
 // maps: Q, K, V, dO (3-D [BH][N][d] 16-bit, 64 x 128 boxes, 128-byte swizzle), then the
 // fp32 dQ accumulator (3-D [BH][N][d], 32 x 128 boxes, 128-byte swizzle).
-cudaError_t launch_bwd_d64_f16(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
-cudaError_t launch_bwd_d64_bf16(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
-cudaError_t launch_bwd_d128_f16(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
-cudaError_t launch_bwd_d128_bf16(bool causal, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
+cudaError_t launch_bwd_d64_f16(bool causal, bool ext, const CUtensorMap* maps, const BwdParams& p,
+                               cudaStream_t s);
+cudaError_t launch_bwd_d64_bf16(bool causal, bool ext, const CUtensorMap* maps, const BwdParams& p,
+                               cudaStream_t s);
+cudaError_t launch_bwd_d128_f16(bool causal, bool ext, const CUtensorMap* maps, const BwdParams& p,
+                               cudaStream_t s);
+cudaError_t launch_bwd_d128_bf16(bool causal, bool ext, const CUtensorMap* maps, const BwdParams& p,
+                               cudaStream_t s);
 cudaError_t launch_bwd_prep(bool bf16, const BwdPrepParams& p, cudaStream_t s);
 cudaError_t launch_bwd_convert(bool bf16, const BwdConvertParams& p, cudaStream_t s);
 

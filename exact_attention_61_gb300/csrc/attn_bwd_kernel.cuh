@@ -193,7 +193,9 @@ struct BwdCfg {
     static constexpr int kWarpLoad = 13;
 };
 
-template <int D, bool CAUSAL, bool BF16>
+// EXT: key padding, a window and Nq != Nk (the forward's EXT readings); without it the
+// code for them is compiled out and Nq = Nk, top-left.
+template <int D, bool CAUSAL, bool BF16, bool EXT>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -217,10 +219,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // Heaviest key tiles first: under the causal mask key tile 0 sees every Q tile.
     const int bh = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.BH));
     const int kt = static_cast<int>(blockIdx.x / static_cast<uint32_t>(p.BH));
-    const int N = p.N;
+    const int Nq = p.Nq, Nk = p.Nk;
     const int j0 = kt * 128;
-    const int qt0 = CAUSAL ? kt : 0;
-    const int n_it = p.n_tiles - qt0;  // >= 1
+    // Valid keys of this batch element; key j is visible to query row i iff j < n_b and,
+    // with the causal mask, j <= i + up and, with a left window, j >= i + lo.
+    const int n_b = (EXT && p.kv_lens) ? min(max(p.kv_lens[bh / p.H], 0), Nk) : Nk;
+    const int diag_off = (EXT && p.align_br) ? n_b - Nq : 0;
+    const int up = diag_off + (EXT ? p.win_right : 0);
+    const bool has_lo = EXT && p.win_left >= 0;
+    const int lo = diag_off - (EXT ? p.win_left : 0);
+    // The Q tiles that see at least one key of this tile.
+    const int n_qt = p.Npad / 128;
+    int qt_begin = 0, qt_end = n_qt;
+    if (CAUSAL) {
+        const int i_min = j0 - up;  // first row that sees key j0
+        qt_begin = i_min <= 0 ? 0 : min(n_qt, i_min / 128);
+    }
+    if (has_lo) {
+        const int i_max = min(j0 + 127, n_b - 1) - lo;  // last row that sees the last valid key
+        qt_end = i_max < 0 ? 0 : min(n_qt, i_max / 128 + 1);
+    }
+    if (j0 >= n_b) qt_end = qt_begin;  // no valid key here: dK = dV = 0
+    const int qt0 = qt_begin;
+    const int n_it = max(0, qt_end - qt_begin);
     WaitCtx wc{p.err, misc + 1, blockIdx.x};
 
     if (threadIdx.x == 0) {
@@ -425,10 +446,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const float* vec = reinterpret_cast<const float*>(smem_bwd + C::kOffVec + s * C::kVecBytes);
             const float* nlse2 = vec + 64 * h;        // -LSE log2(e) of this half's query rows
             const float* ndvec = vec + 128 + 64 * h;  // -D
-            const bool diag = CAUSAL && q0 == j0;  // only this Q tile has keys after queries
-            const bool key_out = j >= N;           // padded key row: P = 0
-            // causal: on the diagonal tile key r sees query columns >= r only
-            const bool mask_tile = key_out || diag;
+            const bool key_out = j >= n_b;  // padded (or past Nk) key row: P = 0
+            // Whether some query row of this tile may not see this thread's key.
+            const bool mask_tile = key_out || (CAUSAL && j > q0 + up) || (has_lo && j < q0 + 127 + lo);
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 const uint32_t col32 = 64u * h + 32u * c;  // first fp32 column of this chunk
@@ -451,10 +471,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                                                  qk2, make_float2(nl.z, nl.w));
                     float pe[4] = {ex2_ftz(y0.x), ex2_ftz(y0.y), ex2_ftz(y1.x), ex2_ftz(y1.y)};
                     if (mask_tile) {
-                        const int qcol = 64 * static_cast<int>(h) + col;  // within the Q tile
+                        const int q = q0 + 64 * static_cast<int>(h) + col;  // query row of pe[0]
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            if (key_out || static_cast<int>(r) > qcol + k) pe[k] = 0.f;
+                            if (key_out || (CAUSAL && j > q + k + up) || (has_lo && j < q + k + lo)) pe[k] = 0.f;
                     }
                     const float2 p0 = make_float2(pe[0], pe[1]), p1 = make_float2(pe[2], pe[3]);
                     const float2 ds0 = __fmul2_rn(
@@ -491,9 +511,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
         }
         // ---- epilogue: dV and dK of this thread's key, columns [d/2 h, d/2 (h+1)) -----
+        // A key tile no query row sees (EXT only) stores zeros: its TMEM was never written.
         if (ok) ok = wait_warp(bar(C::kBarAcc), 0, wc, kRoleBwdCompute * 1000 + C::kBarAcc, n_it);
         if (ok) {
-            tc_fence_after_sync();
+            const bool any = n_it > 0;
+            if (any) tc_fence_after_sync();
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = which == 0 ? C::colDV : C::colDK;
@@ -502,11 +524,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll 1
                 for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + col + 32 * c, o);
-                    tmem_ld_wait();
-                    reg_fence(o);
-                    if (j < N) {
-                        uint4* row = reinterpret_cast<uint4*>(out + ((static_cast<size_t>(bh) * N + j) * D + 32 * c) * 2);
+                    if (any) {
+                        tmem_ld32(lane_base + col + 32 * c, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
+                    if (j < Nk) {
+                        uint4* row = reinterpret_cast<uint4*>(out + ((static_cast<size_t>(bh) * Nk + j) * D + 32 * c) * 2);
 #pragma unroll
                         for (int e = 0; e < 32; e += 8)
                             row[e >> 3] = make_uint4(

@@ -388,8 +388,8 @@ struct BwdArgs {
     const float* lse;
     const void* dout;
     void *dq, *dk, *dv;
-    int64_t B, H, N, d;
-    int causal;
+    int64_t B, H, Nq, Nk, d;
+    MaskSpec ms;
     float scale;
     int dtype;
     void* ws;
@@ -400,7 +400,7 @@ struct BwdArgs {
 int bwd_validate(const BwdArgs& a) {
     if (!a.q || !a.k || !a.v || !a.o || !a.lse || !a.dout || !a.dq || !a.dk || !a.dv || !a.ws)
         return ATTN_ERR_INVALID_ARG;
-    if (a.B < 1 || a.H < 1 || a.N < 1 || a.d < 1) return ATTN_ERR_INVALID_ARG;
+    if (a.B < 1 || a.H < 1 || a.Nq < 1 || a.Nk < 1 || a.d < 1) return ATTN_ERR_INVALID_ARG;
     if (a.dtype != ATTN_FP16 && a.dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (a.d != 64 && a.d != 128) return ATTN_ERR_UNSUPPORTED;
@@ -408,19 +408,22 @@ int bwd_validate(const BwdArgs& a) {
     for (const void* p : ptrs)
         if (reinterpret_cast<uintptr_t>(p) % 16u) return ATTN_ERR_MISALIGNED;
     const int64_t lim31 = (int64_t(1) << 31) - 1;
-    if (a.B > lim31 || a.H > lim31 || a.N > lim31 || a.B * a.H > lim31) return ATTN_ERR_UNSUPPORTED;
+    if (a.B > lim31 || a.H > lim31 || a.Nq > lim31 || a.Nk > lim31 || a.B * a.H > lim31)
+        return ATTN_ERR_UNSUPPORTED;
     const int64_t BH = a.B * a.H;
-    if (BH > (int64_t(1) << 60) / (a.N * a.d)) return ATTN_ERR_UNSUPPORTED;
-    const BwdLayout L = bwd_layout(BH, a.N, a.d);
-    if ((L.Npad / kBwdTile) * BH > lim31) return ATTN_ERR_UNSUPPORTED;
+    const int64_t Nmax = a.Nq > a.Nk ? a.Nq : a.Nk;
+    if (BH > (int64_t(1) << 60) / (Nmax * a.d)) return ATTN_ERR_UNSUPPORTED;
+    const BwdLayout L = bwd_layout(BH, a.Nq, a.d);
+    if (((a.Nk + kBwdTile - 1) / kBwdTile) * BH > lim31) return ATTN_ERR_UNSUPPORTED;
     if (a.ws_bytes < L.bytes) return ATTN_ERR_INVALID_ARG;
-    const uint64_t t = static_cast<uint64_t>(BH * a.N * a.d) * 2u;
-    const uint64_t lb = static_cast<uint64_t>(BH * a.N) * 4u;
+    const uint64_t tq = static_cast<uint64_t>(BH * a.Nq * a.d) * 2u;  // q, o, dout, dq
+    const uint64_t tk = static_cast<uint64_t>(BH * a.Nk * a.d) * 2u;  // k, v, dk, dv
+    const uint64_t lb = static_cast<uint64_t>(BH * a.Nq) * 4u;
     // outputs (dq, dk, dv, workspace) overlap nothing
     const void* outs[4] = {a.dq, a.dk, a.dv, a.ws};
-    const uint64_t osz[4] = {t, t, t, L.bytes};
+    const uint64_t osz[4] = {tq, tk, tk, L.bytes};
     const void* all[10] = {a.q, a.k, a.v, a.o, a.lse, a.dout, a.dq, a.dk, a.dv, a.ws};
-    const uint64_t asz[10] = {t, t, t, t, lb, t, t, t, t, L.bytes};
+    const uint64_t asz[10] = {tq, tk, tk, tq, lb, tq, tq, tk, tk, L.bytes};
     for (int i = 0; i < 4; ++i)
         for (int j = 0; j < 10; ++j)
             if (all[j] != outs[i] && ranges_overlap(outs[i], osz[i], all[j], asz[j])) return ATTN_ERR_INVALID_ARG;
@@ -446,21 +449,22 @@ int bwd_impl(const BwdArgs& a) {
     uint32_t* status = status_ptr(dev, &e);
     if (!status) return cuda_fail(e);
     const int64_t BH = a.B * a.H;
-    const BwdLayout L = bwd_layout(BH, a.N, a.d);
+    const BwdLayout L = bwd_layout(BH, a.Nq, a.d);
     char* ws = static_cast<char*>(a.ws);
     float* lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
     float* dvec = reinterpret_cast<float*>(ws + L.dvec_off);
     float* dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
     alignas(64) CUtensorMap maps[5];
     const void* ptrs[4] = {a.q, a.k, a.v, a.dout};
+    const int64_t rows[4] = {a.Nq, a.Nk, a.Nk, a.Nq};
     for (int i = 0; i < 5; ++i) {
         CUresult r;
         if (i < 4) {
-            r = make_map(enc, &maps[i], ptrs[i], BH, a.N, a.d, a.dtype);
+            r = make_map(enc, &maps[i], ptrs[i], BH, rows[i], a.d, a.dtype);
         } else {  // fp32 dQ accumulator, 32-column boxes (128 bytes: the swizzle span)
-            const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.d), static_cast<cuuint64_t>(a.N),
+            const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.d), static_cast<cuuint64_t>(a.Nq),
                                         static_cast<cuuint64_t>(BH)};
-            const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.d * 4), static_cast<cuuint64_t>(a.N * a.d * 4)};
+            const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.d * 4), static_cast<cuuint64_t>(a.Nq * a.d * 4)};
             const cuuint32_t box[3] = {32, 128, 1};
             const cuuint32_t estr[3] = {1, 1, 1};
             r = enc(&maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, dims, strides, box, estr,
@@ -475,7 +479,7 @@ int bwd_impl(const BwdArgs& a) {
     const bool bf16 = a.dtype == ATTN_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(a.stream);
 
-    BwdPrepParams pp{a.o, a.dout, a.lse, lse2, dvec, dq_acc, static_cast<int>(a.N), static_cast<int>(L.Npad),
+    BwdPrepParams pp{a.o, a.dout, a.lse, lse2, dvec, dq_acc, static_cast<int>(a.Nq), static_cast<int>(L.Npad),
                      static_cast<int>(BH), static_cast<int>(a.d)};
     e = launch_bwd_prep(bf16, pp, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -487,20 +491,28 @@ int bwd_impl(const BwdArgs& a) {
     p.dk = a.dk;
     p.dv = a.dv;
     p.err = status;
-    p.N = static_cast<int>(a.N);
+    p.Nq = static_cast<int>(a.Nq);
+    p.Nk = static_cast<int>(a.Nk);
     p.Npad = static_cast<int>(L.Npad);
     p.BH = static_cast<int>(BH);
-    p.n_tiles = static_cast<int>(L.Npad / kBwdTile);
+    p.H = static_cast<int>(a.H);
+    p.n_ktiles = static_cast<int>((a.Nk + kBwdTile - 1) / kBwdTile);
+    p.kv_lens = a.ms.kv_lens;
+    p.align_br = a.ms.align_br;
+    p.win_right = a.ms.win_right;
+    p.win_left = a.ms.win_left;
     p.qk_scale = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.scale = a.scale;
-    const bool c = a.causal != 0;
+    const bool c = a.ms.causal;
+    // Padding, a window or Nq != Nk need the extended instances.
+    const bool x = a.ms.kv_lens != nullptr || a.ms.win_left >= 0 || a.ms.win_right != 0 || a.Nq != a.Nk;
     if (a.d == 64)
-        e = bf16 ? launch_bwd_d64_bf16(c, maps, p, s) : launch_bwd_d64_f16(c, maps, p, s);
+        e = bf16 ? launch_bwd_d64_bf16(c, x, maps, p, s) : launch_bwd_d64_f16(c, x, maps, p, s);
     else
-        e = bf16 ? launch_bwd_d128_bf16(c, maps, p, s) : launch_bwd_d128_f16(c, maps, p, s);
+        e = bf16 ? launch_bwd_d128_bf16(c, x, maps, p, s) : launch_bwd_d128_f16(c, x, maps, p, s);
     if (e != cudaSuccess) return cuda_fail(e);
 
-    BwdConvertParams cp{dq_acc, a.dq, a.scale, static_cast<long long>(BH * a.N * a.d)};
+    BwdConvertParams cp{dq_acc, a.dq, a.scale, static_cast<long long>(BH * a.Nq * a.d)};
     e = launch_bwd_convert(bf16, cp, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
@@ -598,17 +610,42 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d) {
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
              void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
              int dtype, void* workspace, size_t workspace_bytes, void* stream) {
-    const BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, dtype, workspace,
-                    workspace_bytes, stream};
+    const BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, N, N, d, mask_of(causal ? ATTN_MASK_CAUSAL : ATTN_MASK_NONE),
+                    scale, dtype, workspace, workspace_bytes, stream};
     return bwd_impl(a);
+}
+
+int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                    int64_t d, int64_t window_left, int64_t window_right, const int32_t* kv_lens, int align,
+                    float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, MaskSpec{}, scale, dtype, workspace,
+              workspace_bytes, stream};
+    const int st = window_spec(Nq, Nk, window_left, window_right, kv_lens, align, &a.ms);
+    if (st != ATTN_OK) return st;
+    return bwd_impl(a);
+}
+
+int attn_bwd_window_checked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t Nq,
+                            int64_t Nk, int64_t d, int64_t window_left, int64_t window_right,
+                            const int32_t* kv_lens, int align, float scale, int dtype, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, MaskSpec{}, scale, dtype, workspace,
+              workspace_bytes, stream};
+    int st = window_spec(Nq, Nk, window_left, window_right, kv_lens, align, &a.ms);
+    if (st != ATTN_OK) return st;
+    st = bwd_validate(a);
+    if (st != ATTN_OK) return st;
+    return checked(run_bwd, &a, q, stream);
 }
 
 int attn_bwd_checked(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
                      int64_t d, int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
                      void* stream) {
-    BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, dtype, workspace,
-              workspace_bytes, stream};
+    BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, B, H, N, N, d, mask_of(causal ? ATTN_MASK_CAUSAL : ATTN_MASK_NONE),
+              scale, dtype, workspace, workspace_bytes, stream};
     const int st = bwd_validate(a);
     if (st != ATTN_OK) return st;
     return checked(run_bwd, &a, q, stream);

@@ -231,9 +231,35 @@ int attn_bwd_checked(const void* q, const void* k, const void* v, const void* o,
                      int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
                      int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
-/* attn_bwd_workspace_bytes -- workspace attn_bwd needs for these sizes: 8 bytes per
- * row padded to 128 rows, plus 4*d bytes per row (0 for sizes attn_bwd rejects).
- * Pure host arithmetic, no CUDA call. */
+/*
+ * attn_bwd_window -- the backward of attn_fwd_window: Nq query rows against Nk keys
+ * with key padding, a sliding window and the diagonal alignment, each row over
+ * exactly the keys the forward lets it see (same arguments and readings as
+ * attn_fwd_window). q, o, dout, dq: [B, H, Nq, d]; k, v, dk, dv: [B, H, Nk, d];
+ * lse [B, H, Nq] from attn_fwd_window with the same arguments.
+ *  - Rows that see no key get dQ = 0; padded keys get dK = dV = 0.
+ *  - The workspace is attn_bwd_workspace_bytes(B, H, Nq, d) bytes.
+ *  - Everything else as attn_bwd.
+ */
+int attn_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                    int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                    int64_t window_left, int64_t window_right, const int32_t* kv_lens,
+                    int align, float scale, int dtype, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* attn_bwd_window_checked -- attn_bwd_window, then synchronise and read the device
+ * status word, as attn_fwd_checked. */
+int attn_bwd_window_checked(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk,
+                            void* dv, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                            int64_t d, int64_t window_left, int64_t window_right,
+                            const int32_t* kv_lens, int align, float scale, int dtype,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_bwd_workspace_bytes -- workspace attn_bwd needs for these sizes (N = the query
+ * rows; for attn_bwd_window pass Nq): 8 bytes per row padded to 128 rows, plus 4*d
+ * bytes per row (0 for sizes attn_bwd rejects). Pure host arithmetic, no CUDA call. */
 size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
 /*

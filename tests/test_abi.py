@@ -95,7 +95,7 @@ def test_headers_declare_the_kv_forward():
     names = _declared_symbols()
     for n in ("attn_fwd_kv", "attn_fwd_kv_checked", "attn_fwd_kv_workspace_bytes", "attn_bwd",
               "attn_bwd_checked", "attn_bwd_workspace_bytes", "attn_fwd_window",
-              "attn_fwd_window_checked"):
+              "attn_fwd_window_checked", "attn_bwd_window", "attn_bwd_window_checked"):
         assert n in names
 
 
