@@ -31,7 +31,7 @@ ATTN_ERR_MISALIGNED = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_SCRATCH_TOO_SMALL = 6
-STATIC_SCRATCH_BYTES = 8 << 20  # scratch of attn_fwd_kv_static
+STATIC_SCRATCH_BYTES = 16 << 20  # scratch of attn_fwd_kv_static
 
 _lock = threading.Lock()
 _lib = None

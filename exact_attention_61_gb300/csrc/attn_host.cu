@@ -64,10 +64,11 @@ uint32_t* status_ptr(int dev, cudaError_t* err) {
 }
 
 // Scratch of attn_fwd_kv_static: split partials live in this file-scope array instead
-// of caller memory. A plan needs B*H * splits * Nq * (d+1) * 4 bytes, and keys are split
-// only while B*H * ceil(Nq/256) < 304 with B*H * splits < 304 + B*H, so 8 MiB holds
-// every plan with Nq <= 16 (at most 607 * 16 * 129 * 4 bytes, about 5 MB).
-constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+// of caller memory. A plan needs B*H * splits * Nq * (d+1) * 4 bytes; keys are split only
+// while B*H * ceil(Nq/256) < 304, into at most ceil(8*152 / (B*H)) ranges, so
+// B*H * splits < 1216 + 304 and 16 MiB holds every plan with Nq <= 16 (at most
+// 1520 * 16 * 129 * 4 bytes, about 12.5 MB).
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_kv_scratch[kStaticScratchBytes];
 
 // Device address of g_kv_scratch on the current device (looked up once per device).
@@ -167,9 +168,15 @@ cudaError_t select_device_of(const void* ptr, int* dev_out) {
     return cudaSuccess;
 }
 
-// Split of the keys over CTAs for few query rows (decoding): aim for two CTAs per SM
-// of a 152-SM GB300, at least one key tile per split, limited by the workspace.
+// Split of the keys over CTAs for few query rows (decoding). Only while the query rows
+// alone give fewer than two CTAs per SM of a 152-SM GB300. The number of ranges S
+// minimises a wave model of the launch: one CTA fits per SM, so the time is about
+// ceil(CTAs * S / 152) waves of (tiles per range + 2) tile times, the 2 standing for a
+// CTA's set-up and epilogue. At most eight waves of CTAs (beyond that a longer launch
+// gains little and the workspace grows); limited by the workspace; S = 1: no split.
 constexpr int64_t kSplitTargetCtas = 2 * 152;
+constexpr int64_t kSmCount = 152;
+constexpr int64_t kCtaCostTiles = 2;
 
 SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes) {
     SplitPlan pl{1, 0, 0, 0};
@@ -177,12 +184,21 @@ SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_by
     pl.tiles_per_split = n_kv_all;
     const int64_t ctas = ((Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta) * BH;
     if (ctas >= kSplitTargetCtas) return pl;  // enough CTAs already
-    int64_t want = (kSplitTargetCtas + ctas - 1) / ctas;
-    want = std::min<int64_t>(std::min<int64_t>(want, n_kv_all), 65535);
-    if (want <= 1) return pl;
     const uint64_t per_split = static_cast<uint64_t>(BH) * Nq * (d + 1) * 4u;
     const int64_t fit = static_cast<int64_t>(ws_bytes / per_split);
-    const int64_t n = std::min(want, fit);
+    const int64_t cap = (8 * kSmCount + ctas - 1) / ctas;
+    const int64_t lim = std::min<int64_t>(std::min<int64_t>(std::min<int64_t>(n_kv_all, 65535), fit), cap);
+    auto waves = [&](int64_t c) { return (c + kSmCount - 1) / kSmCount; };
+    int64_t n = 1;
+    int64_t best = waves(ctas) * (n_kv_all + kCtaCostTiles);
+    for (int64_t c = 2; c <= lim; ++c) {
+        const int64_t t = (n_kv_all + c - 1) / c;  // tiles per range
+        const int64_t cost = waves(ctas * ((n_kv_all + t - 1) / t)) * (t + kCtaCostTiles);
+        if (cost < best) {
+            best = cost;
+            n = c;
+        }
+    }
     if (n <= 1) return pl;
     const int64_t tps = (n_kv_all + n - 1) / n;
     pl.tiles_per_split = tps;
@@ -660,7 +676,7 @@ const char* attn_strerror(int status) {
         case ATTN_ERR_CUDA: return "CUDA error (see attn_last_cuda_error)";
         case ATTN_ERR_TIMEOUT: return "device-side wait timed out (outputs undefined)";
         case ATTN_ERR_SCRATCH_TOO_SMALL:
-            return "the split of the keys needs more than the 8 MiB static scratch of attn_fwd_kv_static "
+            return "the split of the keys needs more than the 16 MiB static scratch of attn_fwd_kv_static "
                    "(use attn_fwd_kv with a workspace)";
         default: return "unknown status";
     }

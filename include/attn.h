@@ -129,8 +129,9 @@ int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float
  *    sees no key (bottom-right with Nq > Nk) gets O = 0 and LSE = -inf.
  *  - workspace: optional DEVICE scratch owned by the caller (16-byte aligned,
  *    not overlapping the other arrays; NULL or 0 bytes allowed). When the
- *    query rows alone give too few CTAs for the GPU, the keys are split into
- *    ranges processed by separate CTAs whose fp32 partial outputs and
+ *    query rows alone give too few CTAs for the GPU (fewer than two per SM),
+ *    the keys may be split into ranges (as many as a wave model of the launch
+ *    favours, at most eight waves of CTAs) processed by separate CTAs whose fp32 partial outputs and
  *    log-sum-exps go to the workspace and are merged by a second kernel on the
  *    same stream; how many ranges is bounded by workspace_bytes, and with too
  *    little workspace the call runs unsplit (same results up to fp32
@@ -264,13 +265,13 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
 /*
  * attn_fwd_kv_static -- attn_fwd_kv that allocates nothing and takes no
- * workspace: the split partials go to a static device array of 8 MiB
- * (8388608 bytes) inside this library. The
+ * workspace: the split partials go to a static device array of 16 MiB
+ * (16777216 bytes) inside this library. The
  * pages have no counterpart; it exists for callers that must not allocate or
  * pass device scratch on the call path.
  *  - Arguments, masks and results as attn_fwd_kv. Sizes whose full split of
  *    the keys needs more than the scratch (attn_fwd_kv_workspace_bytes(...) >
- *    8388608) are rejected with ATTN_ERR_SCRATCH_TOO_SMALL before anything is
+ *    16777216) are rejected with ATTN_ERR_SCRATCH_TOO_SMALL before anything is
  *    enqueued. Every size with Nq <= 16 fits.
  *  - Nothing in the scratch needs to start at zero: each call writes every
  *    partial it reads before reading it.

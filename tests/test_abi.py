@@ -132,23 +132,33 @@ def _splits(attn, B, H, Nq, Nk, d):
 @pytest.mark.parametrize("B,H,Nq,Nk,d", [
     (1, 8, 1, 8192, 128), (8, 32, 1, 32768, 64), (1, 1, 1, 128, 64), (1, 1, 1, 129, 64),
     (2, 4, 16, 65536, 128), (1, 16, 300, 20000, 64), (4, 16, 4096, 4096, 64), (1, 1, 5, 100, 64),
+    (8, 32, 1, 8192, 128), (16, 16, 4, 4096, 64), (1, 16, 1, 65536, 128),
 ])
 def test_workspace_split_plan(lib, B, H, Nq, Nk, d):
-    """The split of the keys: none when the query rows already give two CTAs per SM of
-    a 152-SM GPU or when there is a single key tile; else at least two non-empty ranges
-    of 128-key tiles, enough to reach that target when the keys allow."""
+    """The split of the keys: none when the query rows already give two CTAs per SM of a
+    152-SM GPU; otherwise the range count minimises ceil(CTAs * S / 152) waves of
+    (tiles per range + 2) tile times over every count up to eight waves of CTAs, with no
+    empty range (brute force over all counts here)."""
     from exact_attention_61_gb300 import attn
     ctas = -(-Nq // 256) * B * H
     n_kv = -(-Nk // 128)
     S = _splits(attn, B, H, Nq, Nk, d)
-    if ctas >= 304 or n_kv == 1:
+    if ctas >= 304:
         assert S == 0
+        return
+
+    def cost(c):
+        t = -(-n_kv // c)
+        return -(-ctas * -(-n_kv // t) // 152) * (t + 2)
+
+    best = min(cost(c) for c in range(1, min(n_kv, -(-8 * 152 // ctas)) + 1))
+    if S == 0:  # no split
+        assert cost(1) == best
         return
     assert 2 <= S <= n_kv
     tps = -(-n_kv // S)
     assert (S - 1) * tps < n_kv <= S * tps  # no empty range
-    want = min(n_kv, -(-304 // ctas))
-    assert want / 2 <= S <= want  # whole tiles per range: at most a factor two below the target
+    assert cost(S) == best
 
 
 def test_workspace_bytes_rejects_bad_sizes(lib):
@@ -160,7 +170,7 @@ def test_workspace_bytes_rejects_bad_sizes(lib):
 
 def test_static_scratch_entry_rejects_before_any_cuda_call(lib):
     """attn_fwd_kv_static validates like attn_fwd_kv and refuses sizes whose split needs
-    more than its 8 MiB static scratch, all on the host (fake pointers here)."""
+    more than its 16 MiB static scratch, all on the host (fake pointers here)."""
     from exact_attention_61_gb300 import attn
     args = dict(q=A, k=2 * A * 64, v=3 * A * 64, o=4 * A * 64, lse=5 * A * 64, B=1, H=2, Nq=4,
                 Nk=1000, d=64, mask=2, scale=0.125, dtype=1, stream=None)
