@@ -62,6 +62,9 @@ _BWD_WIN_ARGS = ([ctypes.c_void_p] * 9 + [ctypes.c_int64] * 7 +
                   ctypes.c_void_p])
 
 
+_HOST_ARGS = _FWD_ARGS[:12] + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+
+
 class AttnError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(msg)
@@ -104,6 +107,14 @@ def load(path: str = LIB_PATH):
             lib.attn_bwd_window_checked.restype = ctypes.c_int
             lib.attn_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 4
             lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_fwd_host.argtypes = _HOST_ARGS
+            lib.attn_fwd_host.restype = ctypes.c_int
+            lib.attn_fwd_host_checked.argtypes = _HOST_ARGS
+            lib.attn_fwd_host_checked.restype = ctypes.c_int
+            lib.attn_fwd_host_workspace_bytes.argtypes = [ctypes.c_int64] * 4
+            lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_fwd_host_plan.argtypes = [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_int64)]
+            lib.attn_fwd_host_plan.restype = ctypes.c_int64
             lib.attn_strerror.argtypes = [ctypes.c_int]
             lib.attn_strerror.restype = ctypes.c_char_p
             lib.attn_last_cuda_error.argtypes = []
@@ -154,6 +165,28 @@ def attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream) -> int:
 def attn_fwd_checked(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream) -> int:
     return int(load().attn_fwd_checked(q, k, v, o, lse, B, H, N, d, int(bool(causal)),
                                        float(scale), int(dtype), stream))
+
+
+def attn_fwd_host(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace, workspace_bytes, stream,
+                  checked: bool = False) -> int:
+    """Raw C call of attn_fwd_host (or its checked form) with integer pointers: q, k, v, o,
+    lse in host memory, workspace on the device; returns the attn_status_t."""
+    lib = load()
+    fn = lib.attn_fwd_host_checked if checked else lib.attn_fwd_host
+    return int(fn(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale), int(dtype), workspace,
+                  int(workspace_bytes), stream))
+
+
+def host_workspace_bytes(B, H, N, d) -> int:
+    """Device workspace attn_fwd_host needs (0 for sizes it rejects)."""
+    return int(load().attn_fwd_host_workspace_bytes(B, H, N, d))
+
+
+def host_plan(B, H, N, d) -> Tuple[int, int]:
+    """(number of chunks, heads per chunk) of attn_fwd_host; (0, 0) for rejected sizes."""
+    h = ctypes.c_int64(0)
+    n = int(load().attn_fwd_host_plan(B, H, N, d, ctypes.byref(h)))
+    return n, int(h.value) if n else 0
 
 
 def attn_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, workspace, workspace_bytes,
@@ -210,6 +243,60 @@ def fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, 
     st = call(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N,
               d, causal, scale, _dtype_code(q), stream.cuda_stream)
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def fwd_host(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
+             workspace=None, device=None, stream=None, checked: bool = False) -> Tuple[object, object]:
+    """Attention forward of CPU tensors q, k, v [B, H, N, d] (fp16/bf16, contiguous) through
+    attn_fwd_host: the copies to and from the GPU and the kernels run pipelined by chunks of
+    heads. Returns (o, lse) as CPU tensors (page-locked unless ``out``/``lse`` are given),
+    complete on return: the stream is synchronised. ``workspace`` is a CUDA uint8 tensor of
+    :func:`host_workspace_bytes` bytes (allocated here when not given) on ``device``.
+
+    q = k = v = None reuses the inputs an earlier call staged in ``workspace`` (then ``out``
+    gives the shape and dtype, and ``lse`` and ``workspace`` must be given too)."""
+    import torch
+    if q is None and k is None and v is None:
+        if out is None or lse is None or workspace is None:
+            raise ValueError("reusing staged inputs needs out, lse and workspace")
+        B, H, N, d = out.shape
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        if stream is None:
+            stream = torch.cuda.current_stream(workspace.device)
+        st = attn_fwd_host(None, None, None, out.data_ptr(), lse.data_ptr(), B, H, N, d, causal, scale,
+                           _dtype_code(out), workspace.data_ptr(), workspace.numel(), stream.cuda_stream,
+                           checked=checked)
+        _check(st, "attn_fwd_host")
+        stream.synchronize()
+        return out, lse
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CPU tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    if workspace is None:
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        workspace = torch.empty((host_workspace_bytes(B, H, N, d),), dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    st = attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                       causal, scale, _dtype_code(q), workspace.data_ptr(), workspace.numel(), stream.cuda_stream,
+                       checked=checked)
+    _check(st, "attn_fwd_host")
+    stream.synchronize()
     return out, lse
 
 

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -536,6 +537,240 @@ int bwd_impl(const BwdArgs& a) {
 
 int run_bwd(void* ctx) { return bwd_impl(*static_cast<const BwdArgs*>(ctx)); }
 
+// ---- forward from host buffers -------------------------------------------------------------
+// The heads are processed in chunks: the copy of chunk c+1's q, k, v to the device overlaps
+// the kernel of chunk c, and the copy of chunk c's o and lse back to the host overlaps the
+// kernels after it. Copies run on two library-owned streams (one per direction), the
+// kernels on the caller's stream; events order the three.
+
+constexpr int kHostMaxChunks = 16;
+constexpr int kHostMaxDevices = 64;
+
+struct HostPlan {
+    int64_t heads_per_chunk, n_chunks;
+};
+
+// Chunks of about two full waves of CTAs (one CTA per SM of a 152-SM GB300): a chunk is
+// large enough to fill the GPU, and two waves per chunk keep the waves of the whole
+// problem (which the chunks add up to) near those of one launch. At most 16 chunks.
+HostPlan plan_host(int64_t BH, int64_t N) {
+    const int64_t ctiles = (N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
+    int64_t h = std::max<int64_t>(1, (2 * kSmCount + ctiles - 1) / ctiles);
+    h = std::max<int64_t>(h, (BH + kHostMaxChunks - 1) / kHostMaxChunks);
+    h = std::min<int64_t>(h, BH);
+    return HostPlan{h, (BH + h - 1) / h};
+}
+
+// Device staging of one call inside the caller's workspace: q, k, v, o ([BH][N][d] 16-bit)
+// and lse ([BH][N] fp32), each starting on a 256-byte boundary.
+struct HostLayout {
+    uint64_t q, k, v, o, lse, bytes;
+};
+
+HostLayout host_layout(int64_t BH, int64_t N, int64_t d) {
+    auto up = [](uint64_t x) { return (x + 255u) & ~uint64_t(255); };
+    const uint64_t x = up(static_cast<uint64_t>(BH) * N * d * 2u);
+    HostLayout L;
+    L.q = 0;
+    L.k = x;
+    L.v = 2 * x;
+    L.o = 3 * x;
+    L.lse = 4 * x;
+    L.bytes = 4 * x + up(static_cast<uint64_t>(BH) * N * 4u);
+    return L;
+}
+
+// Sizes for which host_layout cannot overflow (the remaining rules are validate()'s).
+bool host_sizes_ok(int64_t B, int64_t H, int64_t N, int64_t d) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return false;
+    if (B > INT32_MAX || H > INT32_MAX || N > INT32_MAX || B * H > INT32_MAX) return false;
+    return B * H <= (int64_t(1) << 58) / (N * d);
+}
+
+// Library-owned streams and events of one device, made on the first call there and kept
+// for the life of the process. Calls on one device enqueue under `mu`, so an event is
+// never recorded by one call between another call's record of it and its wait on it.
+struct HostCtx {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, h2d_done = nullptr, d2h_done = nullptr;
+    cudaEvent_t in_ready[kHostMaxChunks] = {}, out_ready[kHostMaxChunks] = {};
+
+    cudaError_t init() {
+        if (ready) return cudaSuccess;
+        cudaError_t e = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking);
+        cudaEvent_t* evs[3 + 2 * kHostMaxChunks];
+        int n = 0;
+        evs[n++] = &start;
+        evs[n++] = &h2d_done;
+        evs[n++] = &d2h_done;
+        for (int c = 0; c < kHostMaxChunks; ++c) {
+            evs[n++] = &in_ready[c];
+            evs[n++] = &out_ready[c];
+        }
+        for (int i = 0; i < n && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            for (int i = 0; i < n; ++i)
+                if (*evs[i]) {
+                    cudaEventDestroy(*evs[i]);
+                    *evs[i] = nullptr;
+                }
+            if (h2d) cudaStreamDestroy(h2d);
+            if (d2h) cudaStreamDestroy(d2h);
+            h2d = d2h = nullptr;
+            return e;
+        }
+        ready = true;
+        return cudaSuccess;
+    }
+};
+
+HostCtx g_host_ctx[kHostMaxDevices];
+
+struct HostArgs {
+    const void *q, *k, *v;  // host (or any) memory, [B, H, N, d] of dtype
+    void* o;                // host (or any) memory, [B, H, N, d] of dtype
+    float* lse;             // host (or any) memory, [B, H, N] fp32
+    void* ws;               // device workspace
+    size_t ws_bytes;
+    int64_t B, H, N, d;
+    int causal;
+    float scale;
+    int dtype;
+    void* stream;
+};
+
+// q = k = v = NULL: the inputs are already in the workspace (staged by an earlier call).
+bool host_inputs_staged(const HostArgs& a) { return !a.q && !a.k && !a.v; }
+
+int host_validate(const HostArgs& a, HostLayout* L) {
+    const bool staged = host_inputs_staged(a);
+    if ((!staged && (!a.q || !a.k || !a.v)) || !a.o || !a.lse || !a.ws) return ATTN_ERR_INVALID_ARG;
+    if (a.B < 1 || a.H < 1 || a.N < 1 || a.d < 1) return ATTN_ERR_INVALID_ARG;
+    if (a.d != 64 && a.d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!host_sizes_ok(a.B, a.H, a.N, a.d)) return ATTN_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(a.ws) % 256u) return ATTN_ERR_MISALIGNED;
+    const int64_t BH = a.B * a.H;
+    *L = host_layout(BH, a.N, a.d);
+    if (a.ws_bytes < L->bytes) return ATTN_ERR_INVALID_ARG;
+    // The device staging buffers must pass every rule of attn_fwd.
+    char* w = static_cast<char*>(a.ws);
+    const int st = validate(w + L->q, w + L->k, w + L->v, w + L->o, reinterpret_cast<float*>(w + L->lse), a.B,
+                            a.H, a.N, a.N, a.d, a.causal ? ATTN_MASK_CAUSAL : ATTN_MASK_NONE, a.scale, a.dtype,
+                            nullptr, 0);
+    if (st != ATTN_OK) return st;
+    // Host outputs overlap neither each other, nor the inputs, nor the workspace.
+    const uint64_t qb = static_cast<uint64_t>(BH) * a.N * a.d * 2u, lb = static_cast<uint64_t>(BH) * a.N * 4u;
+    const void* ins[3] = {a.q, a.k, a.v};
+    for (int i = 0; i < 3 && !staged; ++i)
+        if (ranges_overlap(a.o, qb, ins[i], qb) || ranges_overlap(a.lse, lb, ins[i], qb)) return ATTN_ERR_INVALID_ARG;
+    if (ranges_overlap(a.o, qb, a.lse, lb)) return ATTN_ERR_INVALID_ARG;
+    const void* all[5] = {a.o, a.lse, a.q, a.k, a.v};
+    const uint64_t sz[5] = {qb, lb, qb, qb, qb};
+    for (int i = 0; i < (staged ? 2 : 5); ++i)
+        if (ranges_overlap(a.ws, L->bytes, all[i], sz[i])) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+int host_impl(const HostArgs& a) {
+    HostLayout L;
+    const int st0 = host_validate(a, &L);
+    if (st0 != ATTN_OK) return st0;
+    int dev = 0;
+    cudaError_t e = select_device_of(a.ws, &dev);  // the workspace must be device memory
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kHostMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    HostCtx& ctx = g_host_ctx[dev];
+    std::lock_guard<std::mutex> lock(ctx.mu);
+    e = ctx.init();
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    const int64_t BH = a.B * a.H;
+    const HostPlan pl = plan_host(BH, a.N);
+    const uint64_t head = static_cast<uint64_t>(a.N) * a.d * 2u, lhead = static_cast<uint64_t>(a.N) * 4u;
+    char* w = static_cast<char*>(a.ws);
+    const char* hq = static_cast<const char*>(a.q);
+    const char* hk = static_cast<const char*>(a.k);
+    const char* hv = static_cast<const char*>(a.v);
+    char* ho = static_cast<char*>(a.o);
+    char* hl = reinterpret_cast<char*>(a.lse);
+    cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+    const MaskSpec ms = mask_of(a.causal ? ATTN_MASK_CAUSAL : ATTN_MASK_NONE);
+
+    // Everything before this call on `stream` precedes the copies (they may read or
+    // write host buffers that earlier work produces or consumes).
+    e = cudaEventRecord(ctx.start, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaStreamWaitEvent(ctx.h2d, ctx.start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx.d2h, ctx.start, 0);
+    // From here on, whatever happens, `stream` is made to wait for both copy streams
+    // before returning, so that later work on it sees this call's copies finished.
+    int status = ATTN_OK;
+    auto fail = [&](cudaError_t err) {
+        if (status == ATTN_OK) status = cuda_fail(err);
+    };
+    if (e != cudaSuccess) fail(e);
+    const bool staged = host_inputs_staged(a);
+    for (int64_t c = 0; c < pl.n_chunks && status == ATTN_OK && !staged; ++c) {
+        const int64_t h0 = c * pl.heads_per_chunk;
+        const uint64_t off = static_cast<uint64_t>(h0) * head;
+        const uint64_t n = static_cast<uint64_t>(std::min(pl.heads_per_chunk, BH - h0)) * head;
+        e = cudaMemcpyAsync(w + L.q + off, hq + off, n, cudaMemcpyDefault, ctx.h2d);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(w + L.k + off, hk + off, n, cudaMemcpyDefault, ctx.h2d);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(w + L.v + off, hv + off, n, cudaMemcpyDefault, ctx.h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(ctx.in_ready[c], ctx.h2d);
+        if (e != cudaSuccess) fail(e);
+    }
+    int64_t launched = 0;
+    for (int64_t c = 0; c < pl.n_chunks && status == ATTN_OK; ++c) {
+        const int64_t h0 = c * pl.heads_per_chunk;
+        const int64_t hc = std::min(pl.heads_per_chunk, BH - h0);
+        const uint64_t off = static_cast<uint64_t>(h0) * head, loff = static_cast<uint64_t>(h0) * lhead;
+        e = staged ? cudaSuccess : cudaStreamWaitEvent(s, ctx.in_ready[c], 0);
+        if (e != cudaSuccess) {
+            fail(e);
+            break;
+        }
+        // one chunk = hc consecutive (b, h) pairs: a [1, hc, N, d] problem
+        const int st = fwd_core(w + L.q + off, w + L.k + off, w + L.v + off, w + L.o + off,
+                                reinterpret_cast<float*>(w + L.lse + loff), 1, hc, a.N, a.N, a.d, ms, a.scale,
+                                a.dtype, nullptr, 0, s);
+        if (st != ATTN_OK) {
+            status = st;
+            break;
+        }
+        e = cudaEventRecord(ctx.out_ready[c], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx.d2h, ctx.out_ready[c], 0);
+        if (e != cudaSuccess) {
+            fail(e);
+            break;
+        }
+        launched = c + 1;
+    }
+    for (int64_t c = 0; c < launched && status == ATTN_OK; ++c) {
+        const int64_t h0 = c * pl.heads_per_chunk;
+        const int64_t hc = std::min(pl.heads_per_chunk, BH - h0);
+        const uint64_t off = static_cast<uint64_t>(h0) * head, loff = static_cast<uint64_t>(h0) * lhead;
+        // The copy stream has waited for out_ready[c], recorded after chunk c's kernel.
+        e = cudaMemcpyAsync(ho + off, w + L.o + off, static_cast<uint64_t>(hc) * head, cudaMemcpyDefault, ctx.d2h);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(hl + loff, w + L.lse + loff, static_cast<uint64_t>(hc) * lhead, cudaMemcpyDefault,
+                                ctx.d2h);
+        if (e != cudaSuccess) fail(e);
+    }
+    e = cudaEventRecord(ctx.h2d_done, ctx.h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ctx.h2d_done, 0);
+    if (e != cudaSuccess) fail(e);
+    e = cudaEventRecord(ctx.d2h_done, ctx.d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ctx.d2h_done, 0);
+    if (e != cudaSuccess) fail(e);
+    return status;
+}
+
+int run_host(void* ctx) { return host_impl(*static_cast<const HostArgs*>(ctx)); }
+
 }  // namespace
 }  // namespace attn_sm103
 
@@ -665,6 +900,35 @@ int attn_bwd_checked(const void* q, const void* k, const void* v, const void* o,
     const int st = bwd_validate(a);
     if (st != ATTN_OK) return st;
     return checked(run_bwd, &a, q, stream);
+}
+
+int64_t attn_fwd_host_plan(int64_t B, int64_t H, int64_t N, int64_t d, int64_t* heads_per_chunk) {
+    if (!host_sizes_ok(B, H, N, d)) return 0;
+    const HostPlan pl = plan_host(B * H, N);
+    if (heads_per_chunk) *heads_per_chunk = pl.heads_per_chunk;
+    return pl.n_chunks;
+}
+
+size_t attn_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d) {
+    if (!host_sizes_ok(B, H, N, d)) return 0;
+    return static_cast<size_t>(host_layout(B * H, N, d).bytes);
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                  int64_t N, int64_t d, int causal, float scale, int dtype, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+    const HostArgs a{q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, causal, scale, dtype, stream};
+    return host_impl(a);
+}
+
+int attn_fwd_host_checked(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                          int64_t H, int64_t N, int64_t d, int causal, float scale, int dtype, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    HostArgs a{q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, causal, scale, dtype, stream};
+    HostLayout L;
+    const int st = host_validate(a, &L);
+    if (st != ATTN_OK) return st;
+    return checked(run_host, &a, workspace, stream);
 }
 
 const char* attn_strerror(int status) {

@@ -287,6 +287,65 @@ int attn_fwd_kv_static(const void* q, const void* k, const void* v, void* o, flo
                        int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int mask,
                        float scale, int dtype, void* stream);
 
+/*
+ * attn_fwd_host -- attn_fwd for inputs and outputs in HOST memory: copies q, k, v
+ * to the device, runs the forward and copies o and lse back, all enqueued on
+ * `stream`. The pages have no counterpart (their kernels take device tensors);
+ * it is the call for a caller whose arrays live on the host, and it computes
+ * exactly what attn_fwd computes (bit for bit: the same kernel on the same
+ * heads).
+ *  - q, k, v, o: [B, H, N, d] of `dtype`, lse: [B, H, N] fp32, contiguous, in
+ *    host memory (page-locked memory lets the copies overlap the kernels;
+ *    pageable memory works but the copies then block the calling thread). Any
+ *    alignment. o and lse must not overlap each other, the inputs or the
+ *    workspace.
+ *  - q, k and v may all three be NULL: the inputs are then the ones already in
+ *    the workspace, staged there by an earlier attn_fwd_host call with the same
+ *    B, H, N, d and dtype (e.g. to run the other mask on the same inputs without
+ *    copying them again). That call must be ordered before this one, for
+ *    instance by enqueuing both on `stream`. Only o and lse are copied then.
+ *  - workspace: DEVICE memory owned by the caller, 256-byte aligned, of at
+ *    least attn_fwd_host_workspace_bytes(B, H, N, d) bytes; the call runs on
+ *    the device that owns it. It stages the five arrays on the device: nothing
+ *    in it needs initialising, and calls that may run at the same time need
+ *    workspaces of their own. After the call it holds q, k, v, o and lse at
+ *    the offsets of the layout below.
+ *  - Pipelining: the B*H heads are processed in attn_fwd_host_plan() chunks
+ *    of consecutive heads. The copy of chunk c+1's inputs overlaps chunk c's
+ *    kernel and the copy of chunk c's outputs overlaps the kernels after it.
+ *    The copies run on two streams the library creates on the first call on a
+ *    device (with 35 events) and keeps; the kernels run on `stream`. Every
+ *    copy follows the work enqueued on `stream` before the call, and work
+ *    enqueued on `stream` after it follows every copy. o and lse are complete
+ *    once `stream` has reached that point (e.g. after cudaStreamSynchronize).
+ *  - Workspace layout (bytes, each part rounded up to 256): q at 0, k at X,
+ *    v at 2X, o at 3X, lse at 4X, with X = B*H*N*d*2; total 4X + B*H*N*4.
+ *  - Errors: as attn_fwd (with one or two of q, k, v NULL an invalid argument),
+ *    plus ATTN_ERR_INVALID_ARG for a null or too small workspace and ATTN_ERR_MISALIGNED for a workspace not 256-byte aligned,
+ *    all before anything is enqueued. Host threads enqueuing on one device
+ *    are serialised by a lock of the library.
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                  int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_fwd_host_checked -- attn_fwd_host, then synchronise `stream` and read the
+ * device status word, as attn_fwd_checked. */
+int attn_fwd_host_checked(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                          int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_fwd_host_workspace_bytes -- workspace attn_fwd_host needs (layout above);
+ * 0 for sizes it rejects. Pure host arithmetic, no CUDA call. */
+size_t attn_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
+
+/* attn_fwd_host_plan -- the chunks of attn_fwd_host: returns their number (0 for
+ * sizes it rejects) and stores the heads per chunk (the last chunk holds the
+ * rest) in *heads_per_chunk when it is not NULL. A chunk is about two full waves
+ * of CTAs of a 152-SM GPU (ceil(304 / ceil(N/256)) heads), with at most 16
+ * chunks. Pure host arithmetic, no CUDA call. */
+int64_t attn_fwd_host_plan(int64_t B, int64_t H, int64_t N, int64_t d, int64_t* heads_per_chunk);
+
 /* attn_strerror -- static, human-readable text for an attn_status_t. Never NULL. */
 const char* attn_strerror(int status);
 

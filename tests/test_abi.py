@@ -240,3 +240,89 @@ def test_window_host_validation(lib):
         G = 1 << 40  # fake addresses far enough apart for 2^30 keys
         assert f(Nk=1 << 30, q=G, k=2 * G, v=3 * G, o=4 * G, lse=5 * G) == 2  # Nq + Nk beyond 2^30
         assert f(dtype=9) == 1
+
+
+# ---- attn_fwd_host: host-side planning and validation (no CUDA call) ------------------------
+
+def test_headers_declare_the_host_forward():
+    names = _declared_symbols()
+    for n in ("attn_fwd_host", "attn_fwd_host_checked", "attn_fwd_host_workspace_bytes", "attn_fwd_host_plan"):
+        assert n in names
+
+
+@pytest.mark.parametrize("B,H,N,d", [
+    (4, 16, 4096, 64), (1, 1, 1, 64), (1, 1, 100, 128), (32, 16, 512, 64), (1, 16, 8192, 128),
+    (2, 2, 777, 64), (64, 64, 128, 64), (1, 200, 65536, 128), (3, 5, 300, 128), (1024, 1, 256, 64),
+])
+def test_host_plan_covers_every_head(lib, B, H, N, d):
+    from exact_attention_61_gb300 import attn
+    n, h = attn.host_plan(B, H, N, d)
+    BH = B * H
+    ctiles = -(-N // 256)
+    assert 1 <= n <= 16 and 1 <= h <= BH
+    assert (n - 1) * h < BH <= n * h          # the chunks cover [0, BH) once; the last holds the rest
+    if n > 1:
+        # every chunk but the last fills two waves of one CTA per SM of a 152-SM GPU
+        assert h * ctiles >= 2 * 152
+    else:
+        assert h == BH
+    if h * ctiles > 2 * 152 + ctiles:
+        assert n == 16 or h == BH                 # chunks grow past two waves only to stay <= 16
+
+
+def test_host_workspace_layout(lib):
+    from exact_attention_61_gb300 import attn
+    up = lambda x: (x + 255) // 256 * 256
+    for B, H, N, d in ((4, 16, 4096, 64), (1, 1, 1, 64), (2, 3, 77, 128)):
+        X = up(B * H * N * d * 2)
+        assert attn.host_workspace_bytes(B, H, N, d) == 4 * X + up(B * H * N * 4)
+    for bad in ((0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 96), (1 << 31, 1, 1, 64)):
+        assert attn.host_workspace_bytes(*bad) == 0
+        assert attn.host_plan(*bad) == (0, 0)
+
+
+W = 1 << 40  # fake device workspace address (256-byte aligned)
+
+
+def _call_host(lib_mod, checked=False, **kw):
+    B, H, N, d = kw.get("B", 1), kw.get("H", 2), kw.get("N", 128), kw.get("d", 64)
+    ws_n = lib_mod.host_workspace_bytes(B, H, N, d) if d in (64, 128) and min(B, H, N) > 0 else 1 << 20
+    args = dict(q=A, k=2 * A * 64, v=3 * A * 64, o=4 * A * 64, lse=5 * A * 64, B=B, H=H, N=N, d=d, causal=0,
+                scale=0.125, dtype=1, workspace=W, workspace_bytes=ws_n, stream=None)
+    args.update(kw)
+    return lib_mod.attn_fwd_host(**args, checked=checked)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(q=0, k=0), 1), (dict(k=0, v=0), 1),
+    (dict(q=0, k=0, v=0, o=0), 1), (dict(q=0, k=0, v=0, lse=0), 1),
+    (dict(o=0), 1), (dict(lse=0), 1), (dict(workspace=0), 1),
+    (dict(B=0), 1), (dict(N=-1), 1), (dict(dtype=2), 1), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1),
+    (dict(d=96), 2), (dict(B=1 << 31), 2),
+    (dict(workspace=W + 16), 3),                 # the workspace must be 256-byte aligned
+    (dict(workspace_bytes=1000), 1),             # too small
+    (dict(o=A), 1),                              # o aliases q
+    (dict(lse=2 * A * 64 + 64), 1),              # lse inside k
+    (dict(o=4 * A * 64, lse=4 * A * 64 + 512), 1),   # lse inside o
+    (dict(q=W + 4096), 1),                       # an input inside the workspace
+])
+def test_host_entry_validation(lib, kw, status):
+    from exact_attention_61_gb300 import attn
+    assert _call_host(attn, **kw) == status
+    assert _call_host(attn, checked=True, **kw) == status
+
+
+def test_host_entry_accepts_unaligned_host_buffers(lib):
+    """Host buffers need no alignment: an odd address passes validation and the call only
+    fails later, at the CUDA query of the (fake) workspace, with ATTN_ERR_CUDA."""
+    from exact_attention_61_gb300 import attn
+    assert _call_host(attn, q=A + 3, o=4 * A * 64 + 1) == attn.ATTN_ERR_CUDA
+
+
+def test_host_entry_staged_inputs_pass_validation(lib):
+    """q = k = v = NULL (inputs already staged in the workspace) is valid: the call gets as far
+    as the CUDA query of the (fake) workspace and fails there with ATTN_ERR_CUDA."""
+    from exact_attention_61_gb300 import attn
+    assert _call_host(attn, q=0, k=0, v=0) == attn.ATTN_ERR_CUDA
+    assert _call_host(attn, q=0, k=0, v=0, workspace=W + 16) == attn.ATTN_ERR_MISALIGNED
+    assert _call_host(attn, q=0, k=0, v=0, o=W + 256) == attn.ATTN_ERR_INVALID_ARG   # o inside the workspace
