@@ -284,9 +284,9 @@ def fwd_host(q, k, v, causal: bool = False, scale: Optional[float] = None, out=N
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q).pin_memory()
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
     if workspace is None:
         dev = torch.device("cuda") if device is None else torch.device(device)
         workspace = torch.empty((host_workspace_bytes(B, H, N, d),), dtype=torch.uint8, device=dev)
