@@ -126,6 +126,11 @@ def load(path: str = LIB_PATH):
             lib.attn_probe_tile.restype = ctypes.c_int
             lib.attn_probe_wait_timeout.argtypes = [ctypes.c_void_p]
             lib.attn_probe_wait_timeout.restype = ctypes.c_int
+            lib.attn_probe_plan_split.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_size_t, ctypes.c_int64,
+                                                                        ctypes.POINTER(ctypes.c_int64)]
+            lib.attn_probe_plan_split.restype = ctypes.c_int
+            lib.attn_probe_plan_host.argtypes = [ctypes.c_int64] * 3 + [ctypes.POINTER(ctypes.c_int64)]
+            lib.attn_probe_plan_host.restype = ctypes.c_int64
             _lib = lib
     return _lib
 
@@ -186,6 +191,23 @@ def host_plan(B, H, N, d) -> Tuple[int, int]:
     """(number of chunks, heads per chunk) of attn_fwd_host; (0, 0) for rejected sizes."""
     h = ctypes.c_int64(0)
     n = int(load().attn_fwd_host_plan(B, H, N, d, ctypes.byref(h)))
+    return n, int(h.value) if n else 0
+
+
+def plan_split_for(BH, Nq, Nk, d, ws_bytes, sms) -> Tuple[int, int, int]:
+    """(key ranges, key tiles per range, workspace bytes) of attn_fwd_kv's split of the
+    keys on a GPU with `sms` SMs (test hook)."""
+    out = (ctypes.c_int64 * 3)()
+    st = load().attn_probe_plan_split(BH, Nq, Nk, d, ws_bytes, sms, out)
+    if st != ATTN_OK:
+        raise AttnError(st, f"attn_probe_plan_split: {strerror(st)}")
+    return int(out[0]), int(out[1]), int(out[2])
+
+
+def plan_host_for(BH, N, sms) -> Tuple[int, int]:
+    """(chunks, heads per chunk) of attn_fwd_host on a GPU with `sms` SMs (test hook)."""
+    h = ctypes.c_int64(0)
+    n = int(load().attn_probe_plan_host(BH, N, sms, ctypes.byref(h)))
     return n, int(h.value) if n else 0
 
 

@@ -3,6 +3,7 @@
 Translation units (compiled in parallel, then linked into one shared library
 with the CUDA runtime linked statically):
   attn_host.cu                       C ABI, validation, tensor maps, dispatch
+  attn_static_scratch.cu             device scratch of attn_fwd_kv_static (own module)
   probe.cu                           one-tile tensor-core probe (test hook)
   attn_merge.cu                      merge of split-key partials
   attn_fwd_inst.cu x 4               forward kernel, one unit per (d, dtype)
@@ -30,6 +31,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxe
 
 UNITS = [
     ("attn_host.cu", [], "attn_host.o"),
+    ("attn_static_scratch.cu", [], "attn_static_scratch.o"),
     ("probe.cu", [], "probe.o"),
     ("attn_merge.cu", [], "attn_merge.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=0"], "attn_fwd_d64_f16.o"),

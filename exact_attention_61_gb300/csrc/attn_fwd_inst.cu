@@ -4,14 +4,27 @@
 #include <atomic>
 
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_persist.cuh"
 #include "attn_internal.h"
 
 #if !defined(ATTN_INST_D) || !defined(ATTN_INST_BF16)
 #error "compile with -DATTN_INST_D=<64|128> -DATTN_INST_BF16=<0|1>"
 #endif
 
+#ifndef ATTN_PERSIST_PV_BY_WG
+#define ATTN_PERSIST_PV_BY_WG 0
+#endif
+#ifndef ATTN_PERSIST
+#define ATTN_PERSIST 1
+#endif
+
 namespace attn_sm103 {
 namespace {
+
+// Who issues O += P V in the persistent kernel: the softmax warpgroup itself (1) or a
+// dedicated warp after an mbarrier hand-off (0).
+constexpr bool kPersistPvByWg = ATTN_PERSIST_PV_BY_WG != 0;
+constexpr bool kPersistEnabled = ATTN_PERSIST != 0;
 
 template <int D, bool CAUSAL, bool BF16, bool SPLIT, bool EXT>
 cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s) {
@@ -30,6 +43,36 @@ cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s)
     }
     const dim3 grid(static_cast<unsigned>(p.n_ctiles) * static_cast<unsigned>(p.BH),
                     SPLIT ? static_cast<unsigned>(p.n_splits) : 1u);
+    kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], p);
+    return cudaGetLastError();
+}
+
+// The persistent head-dimension-64 forward: one CTA per SM (fewer if there are fewer
+// work items). Its warpgroups rebalance registers with setmaxnreg, which needs the
+// kernel to be launched with exactly kPersistLaunchRegs registers per thread; any
+// other count is refused here rather than risking an increase that cannot be met.
+template <bool CAUSAL, bool BF16>
+cudaError_t launch_persist(const CUtensorMap* m, const FwdParams& p, cudaStream_t s) {
+    using C = PersistCfg;
+    auto* kern = attn_fwd_persist_kernel<CAUSAL, BF16, kPersistPvByWg>;
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kPersistLaunchRegs) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const int sms = device_sm_count(dev);
+    if (sms < 1) return cudaErrorInvalidDevice;
+    const long long items = static_cast<long long>(p.n_ctiles) * p.BH;
+    const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
     kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], p);
     return cudaGetLastError();
 }
@@ -59,6 +102,12 @@ cudaError_t ATTN_LAUNCH_NAME(bool causal, bool split, bool ext, const CUtensorMa
     if (split)
         return causal ? launch_one<kD, true, kBf16, true, false>(maps, p, s)
                       : launch_one<kD, false, kBf16, true, false>(maps, p, s);
+    // The square problem (Nq = Nk, top-left causal mask) at head dimension 64 runs on the
+    // persistent kernel; every other form on the one-item kernel.
+    if constexpr (kD == 64 && kPersistEnabled) {
+        if (p.Nq == p.Nk && p.align_br == 0)
+            return causal ? launch_persist<true, kBf16>(maps, p, s) : launch_persist<false, kBf16>(maps, p, s);
+    }
     return causal ? launch_one<kD, true, kBf16, false, false>(maps, p, s)
                   : launch_one<kD, false, kBf16, false, false>(maps, p, s);
 }

@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include "attn.h"
+#include "attn_probe.h"
 #include "attn_bwd_internal.h"
 #include "attn_internal.h"
 
@@ -62,31 +63,6 @@ uint32_t* status_ptr(int dev, cudaError_t* err) {
     }
     if (dev >= 0 && dev < 64) cache[dev].store(reinterpret_cast<uintptr_t>(p), std::memory_order_release);
     return static_cast<uint32_t*>(p);
-}
-
-// Scratch of attn_fwd_kv_static: split partials live in this file-scope array instead
-// of caller memory. A plan needs B*H * splits * Nq * (d+1) * 4 bytes; keys are split only
-// while B*H * ceil(Nq/256) < 304, into at most ceil(8*152 / (B*H)) ranges, so
-// B*H * splits < 1216 + 304 and 16 MiB holds every plan with Nq <= 16 (at most
-// 1520 * 16 * 129 * 4 bytes, about 12.5 MB).
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;
-static __device__ __align__(256) unsigned char g_kv_scratch[kStaticScratchBytes];
-
-// Device address of g_kv_scratch on the current device (looked up once per device).
-void* static_scratch_ptr(int dev, cudaError_t* err) {
-    static std::atomic<uintptr_t> cache[64];
-    if (dev >= 0 && dev < 64) {
-        uintptr_t v = cache[dev].load(std::memory_order_acquire);
-        if (v) return reinterpret_cast<void*>(v);
-    }
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_kv_scratch);
-    if (e != cudaSuccess) {
-        *err = e;
-        return nullptr;
-    }
-    if (dev >= 0 && dev < 64) cache[dev].store(reinterpret_cast<uintptr_t>(p), std::memory_order_release);
-    return p;
 }
 
 namespace {
@@ -169,27 +145,54 @@ cudaError_t select_device_of(const void* ptr, int* dev_out) {
     return cudaSuccess;
 }
 
+// SMs of a device (looked up once per device), or 0 if the query fails.
+int device_sm_count(int dev) {
+    static std::atomic<int> cache[64];
+    if (dev >= 0 && dev < 64) {
+        const int v = cache[dev].load(std::memory_order_acquire);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_release);
+    return n;
+}
+
+// SMs of the current device for the size queries; a GB300's 152 when there is none.
+int64_t current_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return kDefaultSmCount;
+    }
+    const int n = device_sm_count(dev);
+    if (n < 1) {
+        cudaGetLastError();
+        return kDefaultSmCount;
+    }
+    return n;
+}
+
 // Split of the keys over CTAs for few query rows (decoding). Only while the query rows
-// alone give fewer than two CTAs per SM of a 152-SM GB300. The number of ranges S
-// minimises a wave model of the launch: one CTA fits per SM, so the time is about
-// ceil(CTAs * S / 152) waves of (tiles per range + 2) tile times, the 2 standing for a
-// CTA's set-up and epilogue. At most eight waves of CTAs (beyond that a longer launch
-// gains little and the workspace grows); limited by the workspace; S = 1: no split.
-constexpr int64_t kSplitTargetCtas = 2 * 152;
-constexpr int64_t kSmCount = 152;
+// alone give fewer than two CTAs per SM. The number of ranges S minimises a wave model
+// of the launch: one CTA fits per SM, so the time is about ceil(CTAs * S / sms) waves of
+// (tiles per range + 2) tile times, the 2 standing for a CTA's set-up and epilogue. At
+// most eight waves of CTAs (beyond that a longer launch gains little and the workspace
+// grows); limited by the workspace; S = 1: no split.
 constexpr int64_t kCtaCostTiles = 2;
 
-SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes) {
+SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms) {
     SplitPlan pl{1, 0, 0, 0};
     const int64_t n_kv_all = (Nk + 127) / 128;
     pl.tiles_per_split = n_kv_all;
+    sms = std::max<int64_t>(sms, 1);
     const int64_t ctas = ((Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta) * BH;
-    if (ctas >= kSplitTargetCtas) return pl;  // enough CTAs already
+    if (ctas >= 2 * sms) return pl;  // enough CTAs already
     const uint64_t per_split = static_cast<uint64_t>(BH) * Nq * (d + 1) * 4u;
     const int64_t fit = static_cast<int64_t>(ws_bytes / per_split);
-    const int64_t cap = (8 * kSmCount + ctas - 1) / ctas;
+    const int64_t cap = (8 * sms + ctas - 1) / ctas;
     const int64_t lim = std::min<int64_t>(std::min<int64_t>(std::min<int64_t>(n_kv_all, 65535), fit), cap);
-    auto waves = [&](int64_t c) { return (c + kSmCount - 1) / kSmCount; };
+    auto waves = [&](int64_t c) { return (c + sms - 1) / sms; };
     int64_t n = 1;
     int64_t best = waves(ctas) * (n_kv_all + kCtaCostTiles);
     for (int64_t c = 2; c <= lim; ++c) {
@@ -243,7 +246,9 @@ int fwd_core(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (!status) return cuda_fail(e);
 
     const int64_t BH = B * H;
-    const SplitPlan plan = plan_split(BH, Nq, Nk, d, ws ? ws_bytes : 0);
+    const int64_t sms = device_sm_count(dev);
+    if (sms < 1) return cuda_fail(cudaErrorInvalidDevice);
+    const SplitPlan plan = plan_split(BH, Nq, Nk, d, ws ? ws_bytes : 0, sms);
     alignas(64) CUtensorMap maps[4];
     const void* ptrs[4] = {q, k, v, o};
     const int64_t rows[4] = {Nq, Nk, Nk, Nq};
@@ -550,12 +555,12 @@ struct HostPlan {
     int64_t heads_per_chunk, n_chunks;
 };
 
-// Chunks of about two full waves of CTAs (one CTA per SM of a 152-SM GB300): a chunk is
+// Chunks of about two full waves of 256-row work items (one CTA per SM): a chunk is
 // large enough to fill the GPU, and two waves per chunk keep the waves of the whole
 // problem (which the chunks add up to) near those of one launch. At most 16 chunks.
-HostPlan plan_host(int64_t BH, int64_t N) {
+HostPlan plan_host(int64_t BH, int64_t N, int64_t sms) {
     const int64_t ctiles = (N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
-    int64_t h = std::max<int64_t>(1, (2 * kSmCount + ctiles - 1) / ctiles);
+    int64_t h = std::max<int64_t>(1, (2 * std::max<int64_t>(sms, 1) + ctiles - 1) / ctiles);
     h = std::max<int64_t>(h, (BH + kHostMaxChunks - 1) / kHostMaxChunks);
     h = std::min<int64_t>(h, BH);
     return HostPlan{h, (BH + h - 1) / h};
@@ -688,7 +693,9 @@ int host_impl(const HostArgs& a) {
     if (e != cudaSuccess) return cuda_fail(e);
 
     const int64_t BH = a.B * a.H;
-    const HostPlan pl = plan_host(BH, a.N);
+    const int64_t sms = device_sm_count(dev);
+    if (sms < 1) return cuda_fail(cudaErrorInvalidDevice);
+    const HostPlan pl = plan_host(BH, a.N, sms);
     const uint64_t head = static_cast<uint64_t>(a.N) * a.d * 2u, lhead = static_cast<uint64_t>(a.N) * 4u;
     char* w = static_cast<char*>(a.ws);
     const char* hq = static_cast<const char*>(a.q);
@@ -796,7 +803,7 @@ int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float
 size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d) {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
     if (B > INT32_MAX || H > INT32_MAX || Nq > INT32_MAX || Nk > INT32_MAX || B * H > INT32_MAX) return 0;
-    return static_cast<size_t>(plan_split(B * H, Nq, Nk, d, SIZE_MAX).bytes);
+    return static_cast<size_t>(plan_split(B * H, Nq, Nk, d, SIZE_MAX, current_sm_count()).bytes);
 }
 
 int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
@@ -820,10 +827,16 @@ int attn_fwd_kv_static(const void* q, const void* k, const void* v, void* o, flo
                        void* stream) {
     const int st = validate(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, nullptr, 0);
     if (st != ATTN_OK) return st;
-    if (plan_split(B * H, Nq, Nk, d, SIZE_MAX).bytes > kStaticScratchBytes) return ATTN_ERR_SCRATCH_TOO_SMALL;
+    // Sizes the scratch cannot hold are refused on the host first (with the current
+    // device's SM count), then again for the device that owns q.
+    if (plan_split(B * H, Nq, Nk, d, SIZE_MAX, current_sm_count()).bytes > kStaticScratchBytes)
+        return ATTN_ERR_SCRATCH_TOO_SMALL;
     int dev = 0;
     cudaError_t e = select_device_of(q, &dev);
     if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t sms = device_sm_count(dev);
+    if (sms < 1) return cuda_fail(cudaErrorInvalidDevice);
+    if (plan_split(B * H, Nq, Nk, d, SIZE_MAX, sms).bytes > kStaticScratchBytes) return ATTN_ERR_SCRATCH_TOO_SMALL;
     void* scratch = static_scratch_ptr(dev, &e);
     if (!scratch) return cuda_fail(e);
     return fwd_kv_impl(q, k, v, o, lse, B, H, Nq, Nk, d, mask, scale, dtype, scratch, kStaticScratchBytes,
@@ -904,7 +917,7 @@ int attn_bwd_checked(const void* q, const void* k, const void* v, const void* o,
 
 int64_t attn_fwd_host_plan(int64_t B, int64_t H, int64_t N, int64_t d, int64_t* heads_per_chunk) {
     if (!host_sizes_ok(B, H, N, d)) return 0;
-    const HostPlan pl = plan_host(B * H, N);
+    const HostPlan pl = plan_host(B * H, N, current_sm_count());
     if (heads_per_chunk) *heads_per_chunk = pl.heads_per_chunk;
     return pl.n_chunks;
 }
@@ -947,6 +960,23 @@ const char* attn_strerror(int status) {
 }
 
 int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int attn_probe_plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms,
+                          int64_t out[3]) {
+    if (!out || BH < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128) || sms < 1) return ATTN_ERR_INVALID_ARG;
+    const SplitPlan pl = plan_split(BH, Nq, Nk, d, ws_bytes, sms);
+    out[0] = pl.n_splits;
+    out[1] = pl.tiles_per_split;
+    out[2] = static_cast<int64_t>(pl.bytes);
+    return ATTN_OK;
+}
+
+int64_t attn_probe_plan_host(int64_t BH, int64_t N, int64_t sms, int64_t* heads_per_chunk) {
+    if (BH < 1 || N < 1 || sms < 1) return 0;
+    const HostPlan pl = plan_host(BH, N, sms);
+    if (heads_per_chunk) *heads_per_chunk = pl.heads_per_chunk;
+    return pl.n_chunks;
+}
 
 int attn_device_error_info(int32_t info[4]) {
     if (!info) return ATTN_ERR_INVALID_ARG;

@@ -61,7 +61,18 @@ struct SplitPlan {
     int64_t n_splits, tiles_per_split;
     uint64_t o_part_bytes, bytes;  // workspace: fp32 O partials, then fp32 LSE partials
 };
-SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes);
+SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms);
+
+// SMs of a device (cached per device; 0 if the query fails), and of the current device
+// for the workspace and plan queries (kDefaultSmCount, a GB300's, without a device).
+constexpr int64_t kDefaultSmCount = 152;
+int device_sm_count(int dev);
+int64_t current_sm_count();
+
+// Static scratch of attn_fwd_kv_static (attn_static_scratch.cu): its size, and its device
+// address on device `dev` (current), or null with *err set.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+void* static_scratch_ptr(int dev, cudaError_t* err);
 
 // Host helpers shared by the C-ABI entry points (defined in attn_host.cu).
 int cuda_fail(cudaError_t e);  // records e for attn_last_cuda_error(); returns ATTN_ERR_CUDA

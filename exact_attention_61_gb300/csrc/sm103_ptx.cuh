@@ -391,6 +391,22 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive on a named barrier without waiting for it (the producer side of a hand-off).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Per-warpgroup register budget (every warp of the warpgroup executes the same one).
+// An increase draws on registers that other warpgroups of the CTA gave back.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte
 // swizzled tile (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B when the
 // tile starts 1024-byte aligned).

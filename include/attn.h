@@ -155,8 +155,11 @@ int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, fl
                         void* stream);
 
 /* attn_fwd_kv_workspace_bytes -- the workspace size with which attn_fwd_kv uses
- * its full split of the keys for these sizes (0: it never splits them). Pure
- * host arithmetic, no CUDA call; 0 for sizes attn_fwd_kv rejects. */
+ * its full split of the keys for these sizes on the current device (0: it never
+ * splits them). The split depends on the GPU's SM count, which this looks up once
+ * per device (a GB300's 152 without a device); otherwise host arithmetic. A
+ * smaller workspace is never wrong: the call then splits the keys less. 0 for
+ * sizes attn_fwd_kv rejects. */
 size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d);
 
 /*
@@ -272,7 +275,8 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
  *  - Arguments, masks and results as attn_fwd_kv. Sizes whose full split of
  *    the keys needs more than the scratch (attn_fwd_kv_workspace_bytes(...) >
  *    16777216) are rejected with ATTN_ERR_SCRATCH_TOO_SMALL before anything is
- *    enqueued. Every size with Nq <= 16 fits.
+ *    enqueued. On GPUs of up to 200 SMs (a GB300 has 152) every size with
+ *    Nq <= 16 fits.
  *  - Nothing in the scratch needs to start at zero: each call writes every
  *    partial it reads before reading it.
  *  - No device or host memory is allocated (no cudaMalloc/cudaFree, no
@@ -339,11 +343,12 @@ int attn_fwd_host_checked(const void* q, const void* k, const void* v, void* o, 
  * 0 for sizes it rejects. Pure host arithmetic, no CUDA call. */
 size_t attn_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
-/* attn_fwd_host_plan -- the chunks of attn_fwd_host: returns their number (0 for
- * sizes it rejects) and stores the heads per chunk (the last chunk holds the
- * rest) in *heads_per_chunk when it is not NULL. A chunk is about two full waves
- * of CTAs of a 152-SM GPU (ceil(304 / ceil(N/256)) heads), with at most 16
- * chunks. Pure host arithmetic, no CUDA call. */
+/* attn_fwd_host_plan -- the chunks of attn_fwd_host on the current device: returns
+ * their number (0 for sizes it rejects) and stores the heads per chunk (the last
+ * chunk holds the rest) in *heads_per_chunk when it is not NULL. A chunk is about
+ * two full waves of 256-row work items of the GPU (ceil(2 * SMs / ceil(N/256))
+ * heads, i.e. ceil(304 / ceil(N/256)) on a 152-SM GB300), with at most 16 chunks.
+ * The SM count is looked up once per device (152 without a device). */
 int64_t attn_fwd_host_plan(int64_t B, int64_t H, int64_t N, int64_t d, int64_t* heads_per_chunk);
 
 /* attn_strerror -- static, human-readable text for an attn_status_t. Never NULL. */

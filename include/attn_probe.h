@@ -48,6 +48,21 @@ int attn_probe_tile(const void* q, const void* k, const void* v, const void* p, 
  */
 int attn_probe_wait_timeout(void* stream);
 
+/*
+ * attn_probe_plan_split / attn_probe_plan_host -- the host planners of attn_fwd_kv
+ * (split of the keys over CTAs) and attn_fwd_host (chunks of heads) for a GPU with
+ * `sms` SMs, so that tests can check them for other SM counts without such a GPU.
+ * The entry points themselves plan with the SM count of the device they run on.
+ * Pure host arithmetic.
+ *  plan_split: out[0] = key ranges (1: no split), out[1] = key tiles per range,
+ *              out[2] = workspace bytes the plan uses; `ws_bytes` caps the ranges
+ *              as it does for attn_fwd_kv. Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
+ *  plan_host:  returns the number of chunks and stores the heads per chunk.
+ */
+int attn_probe_plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms,
+                          int64_t out[3]);
+int64_t attn_probe_plan_host(int64_t BH, int64_t N, int64_t sms, int64_t* heads_per_chunk);
+
 #ifdef __cplusplus
 }
 #endif

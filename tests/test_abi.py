@@ -326,3 +326,34 @@ def test_host_entry_staged_inputs_pass_validation(lib):
     assert _call_host(attn, q=0, k=0, v=0) == attn.ATTN_ERR_CUDA
     assert _call_host(attn, q=0, k=0, v=0, workspace=W + 16) == attn.ATTN_ERR_MISALIGNED
     assert _call_host(attn, q=0, k=0, v=0, o=W + 256) == attn.ATTN_ERR_INVALID_ARG   # o inside the workspace
+
+
+def test_planners_follow_the_sm_count(lib):
+    """The split of the keys (attn_fwd_kv) and the chunks of heads (attn_fwd_host) are
+    planned for the SM count of the GPU they run on: the test hooks take it as an argument.
+    Without a device the public queries plan for a GB300's 152 SMs."""
+    from exact_attention_61_gb300 import attn
+    # chunks of about two waves of 256-row items: ceil(2 * SMs / ceil(N / 256)) heads
+    assert attn.plan_host_for(64, 4096, 152) == (4, 19)
+    assert attn.plan_host_for(64, 4096, 76) == (7, 10)
+    assert attn.plan_host_for(64, 4096, 304) == (2, 38)
+    assert attn.plan_host_for(64, 4096, 152) == attn.host_plan(4, 16, 4096, 64)
+    # decode: 8 x 32 single-row heads against 8192 keys are 256 CTAs
+    full = 1 << 40
+    n152, tps152, b152 = attn.plan_split_for(256, 1, 8192, 128, full, 152)
+    assert n152 == 4 and tps152 == 16 and b152 == 256 * 4 * 1 * 129 * 4
+    assert b152 == attn.workspace_bytes(8, 32, 1, 8192, 128)
+    assert attn.plan_split_for(256, 1, 8192, 128, full, 76)[0] == 1   # 256 CTAs already fill 76 SMs twice
+    # 304 SMs hold the 256 CTAs in one wave (no split); 2048 SMs make room for more ranges
+    assert attn.plan_split_for(256, 1, 8192, 128, full, 304)[0] == 1
+    assert attn.plan_split_for(256, 1, 8192, 128, full, 2048)[0] > n152
+    # a workspace that holds three ranges caps the split below the full plan's four
+    assert attn.plan_split_for(256, 1, 8192, 128, 3 * 256 * 129 * 4, 152)[0] <= 3
+    for sms in (1, 16, 132, 148, 152, 160, 200):
+        for BH, Nq, Nk in ((1, 1, 65536), (16, 4, 4096), (300, 16, 1 << 20), (5, 300, 777)):
+            n, tps, nbytes = attn.plan_split_for(BH, Nq, Nk, 64, full, sms)
+            n_kv = (Nk + 127) // 128
+            assert 1 <= n <= n_kv and tps * n >= n_kv and tps * (n - 1) < n_kv
+            assert nbytes == (0 if n == 1 else BH * n * Nq * 65 * 4)
+            if Nq <= 16:
+                assert nbytes <= attn.STATIC_SCRATCH_BYTES

@@ -1,16 +1,10 @@
 """Parity of the CUDA backward (attn_bwd through the C ABI) with the fp64 oracle.
 
 Tolerance, per element, derived from the arithmetic of the path (the pages state
-none for the backward). With u the unit roundoff of the dtype (2^-11 fp16, 2^-8
-bf16) and g = n 2^-24 for the fp32 sums over n terms:
-  - P is rounded to the dtype before dV += P^T dO, and dS before dK and dQ;
-  - D = dO . O is formed from the 16-bit O, so it is off by at most
-    dD_i = sum_t |dO_it| |dO_it - exact| (see _d_error), and dS_ij by P_ij dD_i;
-  - each output is rounded once to the dtype.
-  bound(dV) = (u + g) |P|^T |dO| + u |dV|
-  bound(dK) = scale ((u + g) |dS| + P dD)^T |Q| + u |dK|
-  bound(dQ) = scale ((u + g) |dS| + P dD) |K| + u |dQ|
-Every element must be within twice its bound (plus 1e-6 absolute for exact zeros).
+none for the backward); the bound and its derivation are in oracle/bwd_bound.py:
+P, dS and the outputs rounded to the dtype, fp32 sums, and D = dO . O formed from the
+16-bit O. Every element must be within twice its bound (plus 1e-6 absolute for exact
+zeros).
 """
 import math
 
@@ -20,8 +14,9 @@ import torch
 
 import oracle
 from gen import make_qkv
+from oracle import bwd_bound
 
-U = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}
+U = bwd_bound.U
 DT = {"fp16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -31,30 +26,13 @@ def _inputs(B, H, N, d, dtype, seed, scale_in=1.0):
     return q, k, v, do
 
 
-def _d_error(do64, o_used, o_exact, u):
-    """Bound on |D_gpu - D| when D is formed from o_used instead of the exact O."""
-    return (np.abs(do64) * (np.abs(o_used - o_exact) + u * np.abs(o_exact))).sum(-1)
+_d_error = bwd_bound.d_error
 
 
 def _check(name, got, ref, m, q64, k64, do64, dD, scale, dtype, N):
-    u = U[dtype]
-    g = N * 2.0 ** -24
-    p, ds = m["p"], m["ds"]
-    eds = (u + g) * np.abs(ds) + p * dD[..., None]
-    bounds = {
-        "dv": (u + g) * np.einsum("bhij,bhid->bhjd", p, np.abs(do64)) + u * np.abs(ref["dv"]),
-        "dk": scale * np.einsum("bhij,bhid->bhjd", eds, np.abs(q64)) + u * np.abs(ref["dk"]),
-        "dq": scale * np.einsum("bhij,bhjd->bhid", eds, np.abs(k64)) + u * np.abs(ref["dq"]),
-    }
-    for key in ("dq", "dk", "dv"):
-        x = got[key].to(torch.float64).cpu().numpy()
-        assert np.isfinite(x).all(), f"{name}: non-finite {key}"
-        err = np.abs(x - ref[key])
-        lim = 2.0 * bounds[key] + 1e-6
-        bad = err > lim
-        assert not bad.any(), (
-            f"{name}: {key} {int(bad.sum())} elements over the bound; worst err {err.max():.3e}, "
-            f"at the worst element err/bound = {(err / lim).max():.2f}")
+    bnd = bwd_bound.bounds(ref, m, q64, k64, do64, dD, scale, dtype, N)
+    ok, msg = bwd_bound.check({key: t.to(torch.float64).cpu().numpy() for key, t in got.items()}, ref, bnd)
+    assert ok, f"{name}: {msg}"
 
 
 def _run(attn, q, k, v, do, o, lse, causal, scale):

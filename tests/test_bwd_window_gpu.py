@@ -1,6 +1,6 @@
 """Parity of the windowed / padded / Nq != Nk backward (attn_bwd_window, through the C
 ABI) with the fp64 oracle (oracle.attn_bwd_window), element by element within the
-rounding bound of tests/test_bwd_gpu.py (P, dS, D and the outputs rounded once), with
+rounding bound of oracle/bwd_bound.py (P, dS, D and the outputs rounded once), with
 P and dS materialised under the same visibility mask. Rows that see no key must give
 dQ = 0 exactly and padded keys dK = dV = 0 exactly.
 """
@@ -12,8 +12,8 @@ import torch
 
 import oracle
 from gen import make_qkv_kv
+from oracle import bwd_bound
 
-U = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}
 DT = {"fp16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -48,24 +48,13 @@ def _case(attn, B, H, Nq, Nk, d, dtype, window, lens, align, seed, e2e=False):
     q64, k64, v64, do64 = (oracle.to_f64(t) for t in (q, k, v, do))
     keep = oracle.window_mask(B, Nq, Nk, window[0], window[1], lens, align)
     p, ds = _masked_p_ds(q64, k64, v64, do64, keep, scale)
-    u = U[dtype]
-    g = max(Nq, Nk) * 2.0 ** -24
     o_used = o.to(torch.float64).cpu().numpy()
-    dD = (np.abs(do64) * (np.abs(o_used - o_ref) + u * np.abs(o_ref))).sum(-1)
-    eds = (u + g) * np.abs(ds) + p * dD[..., None]
-    bounds = {
-        "dv": (u + g) * np.einsum("bhij,bhid->bhjd", p, np.abs(do64)) + u * np.abs(ref["dv"]),
-        "dk": scale * np.einsum("bhij,bhid->bhjd", eds, np.abs(q64)) + u * np.abs(ref["dk"]),
-        "dq": scale * np.einsum("bhij,bhjd->bhid", eds, np.abs(k64)) + u * np.abs(ref["dq"]),
-    }
+    dD = bwd_bound.d_error(do64, o_used, o_ref, bwd_bound.U[dtype])
+    bnd = bwd_bound.bounds(ref, {"p": p, "ds": ds}, q64, k64, do64, dD, scale, dtype, max(Nq, Nk))
     name = f"B{B}H{H}q{Nq}k{Nk}d{d}{dtype} w{window} lens{lens} {align}{' e2e' if e2e else ''}"
     got = {"dq": dq, "dk": dk, "dv": dv}
-    for key in ("dq", "dk", "dv"):
-        x = got[key].to(torch.float64).cpu().numpy()
-        assert np.isfinite(x).all(), f"{name}: non-finite {key}"
-        err = np.abs(x - ref[key])
-        lim = 2.0 * bounds[key] + 1e-6
-        assert not (err > lim).any(), f"{name}: {key} {int((err > lim).sum())} over, worst {err.max():.3e}"
+    ok, msg = bwd_bound.check({key: t.to(torch.float64).cpu().numpy() for key, t in got.items()}, ref, bnd)
+    assert ok, f"{name}: {msg}"
     # exact zeros: rows with no key, padded keys
     no_key = ~keep.any(-1)  # [B, Nq]
     rows = np.broadcast_to(no_key[:, None, :], (B, H, Nq))
