@@ -11,9 +11,6 @@
 #error "compile with -DATTN_INST_D=<64|128> -DATTN_INST_BF16=<0|1>"
 #endif
 
-#ifndef ATTN_PERSIST_PV_BY_WG
-#define ATTN_PERSIST_PV_BY_WG 0
-#endif
 #ifndef ATTN_PERSIST
 #define ATTN_PERSIST 1
 #endif
@@ -21,9 +18,6 @@
 namespace attn_sm103 {
 namespace {
 
-// Who issues O += P V in the persistent kernel: the softmax warpgroup itself (1) or a
-// dedicated warp after an mbarrier hand-off (0).
-constexpr bool kPersistPvByWg = ATTN_PERSIST_PV_BY_WG != 0;
 constexpr bool kPersistEnabled = ATTN_PERSIST != 0;
 
 template <int D, bool CAUSAL, bool BF16, bool SPLIT, bool EXT>
@@ -54,7 +48,7 @@ cudaError_t launch_one(const CUtensorMap* m, const FwdParams& p, cudaStream_t s)
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_persist(const CUtensorMap* m, const FwdParams& p, cudaStream_t s) {
     using C = PersistCfg;
-    auto* kern = attn_fwd_persist_kernel<CAUSAL, BF16, kPersistPvByWg>;
+    auto* kern = attn_fwd_persist_kernel<CAUSAL, BF16>;
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

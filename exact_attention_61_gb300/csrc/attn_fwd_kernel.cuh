@@ -13,8 +13,14 @@
 //  - "Round 4 / Causal tile-skipping": key tiles past the diagonal are never
 //    visited; only the diagonal tile and a ragged last tile are masked
 //    (k_pos < N and, when causal, k_pos <= q_pos);
-//  - "Round 4 / The P cast": l sums the fp32 P; P is rounded to the input dtype
-//    for the second product.
+//  - "Round 4 / The P cast": P is rounded to the input dtype for the second product
+//    and l sums the fp32 P (it gives the LSE). The page finds the order makes no
+//    difference for its kernel, which rescales on every tile, so each tile's largest
+//    P is exactly 1. With the lazy rescale below that P can be any value up to 2^8,
+//    and its rounding would stay in the numerator only: an error proportional to |O|
+//    (up to 0.4 % of |O| on the x2-scaled long problem). So O is normalised by l plus
+//    lc, the sum over tiles of (rounded - fp32) of each tile's largest P: one ex2 per
+//    row and tile instead of a second sum over every rounded P.
 //
 // GB300 design (differs from the pages' Triton/Ada kernels):
 //  - one CTA owns 2 x 128 query rows of one (b, h). Each 128-row Q tile has one
@@ -195,6 +201,27 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&h);
     }
+}
+
+// The two 16-bit values of a packed pair, widened exactly to fp32 (bf16: the high 16
+// bits of an fp32; fp16: a conversion).
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        __half2 h = *reinterpret_cast<__half2*>(&w);
+        return __half22float2(h);
+    }
+}
+
+// Rounding of a tile's largest P (the P of its row maximum, computed exactly as the
+// exp loop computes it) to the input dtype: rounded - fp32. Zero for a row with no
+// visible key in the tile (its maximum is -inf).
+template <bool BF16>
+__device__ __forceinline__ float max_p_rounding(float row_max, float qk, float m_use) {
+    const float pm = ex2_ftz(fmaf(row_max, qk, -m_use));
+    return unpack2<BF16>(pack2<BF16>(pm, 0.f)).x - pm;
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -433,7 +460,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         // decoding) skip the softmax arithmetic; their rows of O are never stored.
         const bool warp_has_rows = row0(t) + static_cast<int>(wq * 32u) < Nq;
         float m = -INFINITY;  // running max, log2 units of the scaled scores (possibly stale)
-        float l = 0.f;        // running sum of P (fp32), relative to m
+        float l = 0.f;        // running sum of P (fp32), relative to m: the LSE
+        float lc = 0.f;       // rounding of each tile's largest P, relative to m: O / (l + lc)
         for (int j = 0; j < n_kv(t) && ok; ++j) {
             const int g = jobs.job(t, j);
             const int b = g % C::kSBufs;
@@ -491,6 +519,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             }
             const float2 s2 = __fadd2_rn(sum2[0], sum2[1]);
             l = l * alpha + (s2.x + s2.y);
+            lc = lc * alpha + max_p_rounding<BF16>(row_max, qk, m_use);
             tmem_st32(tS, pk[0]);
             tmem_st32(tS + 32, pk[1]);
             tmem_st_wait();
@@ -542,7 +571,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             ok = wait_warp(bar(C::kBarOFinal + t), 0, wc, role * 1000 + C::kBarOFinal + t, n_kv(t));
         }
         const float m_fin = (m == -INFINITY) ? 0.f : m;
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = l > 0.f ? 1.f / (l + lc) : 0.f;
         const float lse2 = l > 0.f ? m_fin + log2f(l) : -INFINITY;  // log2 units
         if constexpr (SPLIT) {
             // fp32 partials for the merge: O_s = O / l and log2-sum-exp of this key range.

@@ -13,20 +13,20 @@
 //    tile). S of job g reuses the buffer of job g-3 once O += P V of job g-3 has
 //    completed (pv_done); having seen that, warp 8 also hands the K/V ring stage back
 //    to the loader when job g-3 was the last reader of its tile;
-//  - the softmax warpgroup of Q tile t writes P over S and issues its own O_t += P V
-//    (PV_BY_WG): the hand-off from P to the MMA is a 128-thread named barrier rather
-//    than an mbarrier round trip through another warp. With PV_BY_WG = false a
-//    dedicated warp (11) issues every O += P V after an mbarrier hand-off instead;
+//  - the softmax warpgroup of Q tile t writes P (16-bit) over S in TMEM and hands it to
+//    warp 11, which issues every O_t += P V (P from TMEM, V MN-major in SMEM). With
+//    the S and P V issues in two warps, neither issuer's waits and commits hold up the
+//    other's MMAs (one warp issuing both paced the earlier one-item kernel);
 //  - warp 9 loads Q (two buffers, so item a+1's Q lands while item a runs) and the K/V
 //    ring; warp 10 stores O by TMA from the staging tile the softmax warpgroup wrote
 //    and returns the Q buffer to the loader.
 // Registers: the two softmax warpgroups raise their budget (setmaxnreg) to 208 per
 // thread, the warpgroup of single-warp roles lowers its own to 88.
 //
-// Every mbarrier wait is bounded (as in the one-item kernel). The one named barrier (the
-// 128 threads of a softmax warpgroup, once per job) cannot be bounded, so every warp of
-// the warpgroup executes all of its jobs' barriers even after a timeout, doing no
-// work: the counts always match and the CTA always exits.
+// Every mbarrier wait is bounded (as in the one-item kernel): on expiry a role records
+// the error, stops issuing work, drains its copies and MMAs, and the CTA exits. Every
+// parity wait is exact (the barrier is at most one phase short of the awaited one when
+// the wait starts); the reason is given at each barrier that needs one.
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -54,9 +54,8 @@ struct PersistCfg {
     static constexpr int kBarPvDone = kBarSFull + 2 * kSBufs;  // [buf]
     static constexpr int kBarPFull = kBarPvDone + kSBufs;      // [buf] (PV warp mode)
     static constexpr int kBarODone = kBarPFull + kSBufs;       // [tile][2]
-    static constexpr int kBarOFree = kBarODone + 4;            // [tile] (PV warp mode)
-    static constexpr int kBarOStaged = kBarOFree + 2;          // [buf][tile]: O staged for the store warp
-    static constexpr int kBarDrain = kBarOStaged + 4;          // [issuer]: S, WG0, WG1, PV warp
+    static constexpr int kBarOStaged = kBarODone + 4;          // [buf][tile]: O staged for the store warp
+    static constexpr int kBarDrain = kBarOStaged + 4;          // [issuer]: S, P V
     static constexpr int kNumBars = kBarDrain + 4;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -65,7 +64,6 @@ struct PersistCfg {
     static constexpr int kWarpLoad = 9;
     static constexpr int kWarpStore = 10;
     static constexpr int kWarpPv = 11;
-    static constexpr int kIssueLane = 3;  // warp (within a softmax warpgroup) that issues P V
     static constexpr int kRegsSoftmax = 208;
     static constexpr int kRegsOther = 88;
     __device__ static constexpr uint32_t colS(int b) { return 128u * b; }
@@ -113,7 +111,7 @@ __device__ __forceinline__ int persist_item_index(int k, int n_items) {
     return it < n_items ? it : -1;
 }
 
-template <bool CAUSAL, bool BF16, bool PV_BY_WG>
+template <bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
     attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -140,7 +138,7 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t cnt = 1u;
             if (i >= C::kBarPFull && i < C::kBarPFull + C::kSBufs) cnt = 4u;  // one arrive per softmax warp
-            if (i >= C::kBarOFree && i < C::kBarOStaged + 4) cnt = 4u;  // o_free, o_staged
+            if (i >= C::kBarOStaged && i < C::kBarOStaged + 4) cnt = 4u;  // o_staged
             mbar_init(bar(i), cnt);
         }
         misc[1] = 0u;
@@ -307,14 +305,13 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
             if (lane == 0) tma_store_wait_all();
             __syncwarp();
         } else if (warp == C::kWarpPv) {
-            // ================================ P V issuer (PV warp mode) ===================
-            if constexpr (!PV_BY_WG) {
+            // ================================ P V issuer ==================================
+            {
                 constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, 128, C::D, true);
                 const uint64_t dv0 = sdesc_sw128(sV(0), C::kTileBytes, 1024);
                 constexpr uint64_t kStageStep = C::kTileBytes >> 4;
                 int g = 0, Gb = 0;
-                int kk0 = 0, kk1 = 0;      // O += P V issued per Q tile
-                int items0 = 0, items1 = 0;  // items with work per Q tile
+                int kk0 = 0, kk1 = 0;  // O += P V issued per Q tile
                 bool ok = true;
                 int a = 0;
                 for (int it; ok && (it = persist_item_index(a, n_items)) >= 0; ++a) {
@@ -325,15 +322,14 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                         int t, j;
                         jobs.tile_of(jj, t, j);
                         const int b = g % C::kSBufs;
-                        const int items_t = t ? items1 : items0;
-                        if (j == 0 && items_t > 0 &&
-                            !wait_warp(bar(C::kBarOFree + t), (items_t - 1) & 1, wc, kRoleMma * 1000 + C::kBarOFree + t,
-                                       a)) {
-                            ok = false;
-                            break;
-                        }
                         const int Gt = Gb + j;
                         const int s = Gt % C::kStages;
+                        // p_full: one phase per job in this buffer, awaited in job order; the
+                        // next one needs S(g+3) in the buffer, which waits for this O += P V.
+                        // The first O += P V of an item (it overwrites O) also needs the
+                        // previous item's O read out: the softmax warpgroup reads it (and
+                        // waits for the loads) before it writes the item's first P, so
+                        // p_full implies it.
                         if (!wait_warp(bar(C::kBarPFull + b), (g / C::kSBufs) & 1, wc, kRoleMma * 1000 + C::kBarPFull + b,
                                        g) ||
                             !wait_warp(bar(C::kBarVFull + s), (Gt / C::kStages) & 1, wc,
@@ -349,12 +345,10 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                         mma_commit_warp(bar(C::kBarPvDone + b));
                         ++kk;
                     }
-                    if (w.n0 > 0) ++items0;
-                    if (w.n1 > 0) ++items1;
                     Gb += max(w.n0, w.n1);
                 }
-                mma_commit_warp(bar(C::kBarDrain + 3));
-                wait_warp(bar(C::kBarDrain + 3), 0, wc, kRoleMma * 1000 + C::kBarDrain + 3, 0, false);
+                mma_commit_warp(bar(C::kBarDrain + 1));
+                wait_warp(bar(C::kBarDrain + 1), 0, wc, kRoleMma * 1000 + C::kBarDrain + 1, 0, false);
             }
             __syncwarp();
         }
@@ -369,10 +363,6 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
         const uint32_t tO = lane_base + C::colO(t);
         const float qk = p.qk_scale;
         const float2 qk2 = make_float2(qk, qk);
-        const bool issuer = PV_BY_WG && wq == static_cast<uint32_t>(C::kIssueLane);
-        constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, 128, C::D, true);
-        const uint64_t dv0 = sdesc_sw128(sV(0), C::kTileBytes, 1024);
-        constexpr uint64_t kStageStep = C::kTileBytes >> 4;
 
         bool ok = true;
         int kk = 0;          // O_t += P V issued so far (all items)
@@ -388,7 +378,8 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
             const bool warp_has_rows = row0 + static_cast<int>(wq * 32u) < p.Nq;
             const int qb = a & 1;
             float m = -INFINITY;  // running max, log2 units (possibly stale)
-            float l = 0.f;        // running sum of P, relative to m
+            float l = 0.f;        // running sum of P (fp32), relative to m: the LSE
+            float lc = 0.f;       // rounding of each tile's largest P, relative to m: O / (l + lc)
             for (int j = 0; j < nt; ++j) {
                 const int g = g0 + jobs.job(t, j);
                 const int b = g % C::kSBufs;
@@ -437,6 +428,7 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                     }
                     const float2 s2 = __fadd2_rn(sum2[0], sum2[1]);
                     l = l * alpha + (s2.x + s2.y);
+                    lc = lc * alpha + max_p_rounding<BF16>(row_max, qk, m_use);
                     tmem_st32(tS, pk[0]);
                     tmem_st32(tS + 32, pk[1]);
                     tmem_st_wait();
@@ -468,32 +460,11 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                     }
                     tmem_st_wait();
                 }
+                // P of this warp's rows is in TMEM (wait::st above) and ordered before
+                // the arrive; the P V issuer waits for all four warps.
                 tc_fence_before_sync();
-                if constexpr (PV_BY_WG) {
-                    // P of all 128 rows is in TMEM: one thread issues O_t += P V.
-                    named_bar_sync(1 + t, 128);
-                    if (issuer) {
-                        ok = ok && *wc.abort == 0u;
-                        const int Gt = Gb + j;
-                        const int s = Gt % C::kStages;
-                        if (ok)
-                            ok = wait_warp(bar(C::kBarVFull + s), (Gt / C::kStages) & 1, wc,
-                                           role * 1000 + C::kBarVFull + s, g);
-                        if (ok) {
-                            tc_fence_after_sync();
-                            mma_pv128_warp(tmem + C::colO(t), tmem + C::colS(b), dv0 + s * kStageStep, idesc_o,
-                                           j > 0 ? 1u : 0u);
-                            // o_done before pv_done: one thread's commits arrive in
-                            // order, so once the S issuer has seen pv_done of a job, that
-                            // job's o_done has arrived too (the parity waits rely on it).
-                            mma_commit_warp(bar(C::kBarODone + t * 2 + (kk & 1)));
-                            mma_commit_warp(bar(C::kBarPvDone + b));
-                        }
-                    }
-                } else {
-                    __syncwarp();
-                    if (lane == 0 && ok) mbar_arrive(bar(C::kBarPFull + b));
-                }
+                __syncwarp();
+                if (lane == 0 && ok) mbar_arrive(bar(C::kBarPFull + b));
                 ++kk;
             }
 
@@ -509,7 +480,7 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                     ok = wait_warp(bar(C::kBarODone + t * 2 + ((kk - 1) & 1)), ((kk - 1) >> 1) & 1, wc,
                                    role * 1000 + C::kBarODone + t * 2 + 1, kk);
                 const float m_fin = (m == -INFINITY) ? 0.f : m;
-                const float inv_l = l > 0.f ? 1.f / l : 0.f;
+                const float inv_l = l > 0.f ? 1.f / (l + lc) : 0.f;
                 const float lse2 = l > 0.f ? m_fin + log2f(l) : -INFINITY;
                 if (ok && warp_has_rows) {
                     tc_fence_after_sync();
@@ -537,20 +508,10 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0 && ok) {
-                    // O_t has been read: the next item's first O_t += P V may overwrite it.
-                    if constexpr (!PV_BY_WG) mbar_arrive(bar(C::kBarOFree + t));
-                    mbar_arrive(bar(C::kBarOStaged + qb * 2 + t));  // the staging tile is ready
-                }
+                if (lane == 0 && ok) mbar_arrive(bar(C::kBarOStaged + qb * 2 + t));  // ready to store
             }
             g0 += jobs.total();
             Gb += max(w.n0, w.n1);
-        }
-        if constexpr (PV_BY_WG) {
-            if (issuer) {
-                mma_commit_warp(bar(C::kBarDrain + 1 + t));
-                wait_warp(bar(C::kBarDrain + 1 + t), 0, wc, role * 1000 + C::kBarDrain, 0, false);
-            }
         }
         __syncwarp();
     }
