@@ -192,6 +192,30 @@ static __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, 
     return wait_warp_slow(bar, parity, w, where, iter, honor_abort);
 }
 
+// Whole-warp bounded wait for the single-warp MMA issuers: while the phase is pending the
+// warp sleeps in try_wait (up to 20 us per try, resuming when the phase completes) rather
+// than polling, so it takes no issue slots from the softmax warps of its SMSP. The
+// abort flag and the time limit are checked after every try.
+static __device__ __forceinline__ bool wait_warp_sleep(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                uint32_t where, uint32_t iter, bool honor_abort = true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_sleep<20000u>(bar, parity))) return true;
+        uint32_t give_up = 0;
+        if (lane == 0) {
+            if (honor_abort && *w.abort) give_up = 1;
+            else if (global_timer_ns() - t0 > kWaitTimeoutNs) give_up = 2;
+        }
+        give_up = __shfl_sync(0xffffffffu, give_up, 0);
+        if (give_up) {
+            if (lane == 0 && give_up == 2) record_timeout(w, where, iter);
+            return false;
+        }
+    }
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (BF16) {

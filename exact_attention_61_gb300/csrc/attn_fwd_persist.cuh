@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                 const PItem w = persist_item<CAUSAL>(it, p);
                 const int qb = a & 1;
                 for (int t = 0; t < 2 && ok; ++t)
-                    ok = wait_warp(bar(C::kBarQFull + qb * 2 + t), (a >> 1) & 1, wc,
+                    ok = wait_warp_sleep(bar(C::kBarQFull + qb * 2 + t), (a >> 1) & 1, wc,
                                    kRoleMma * 1000 + C::kBarQFull + qb * 2 + t, a);
                 const JobOrder jobs{w.n0, w.n1};
                 const int njobs = jobs.total();
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                     const int Gt = Gb + j;
                     const int s = Gt % C::kStages;
                     const int b = g % C::kSBufs;
-                    if (!wait_warp(bar(C::kBarKFull + s), (Gt / C::kStages) & 1, wc, kRoleMma * 1000 + C::kBarKFull + s,
+                    if (!wait_warp_sleep(bar(C::kBarKFull + s), (Gt / C::kStages) & 1, wc, kRoleMma * 1000 + C::kBarKFull + s,
                                    g)) {
                         ok = false;
                         break;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                     if (g >= C::kSBufs) {
                         // O += P V of job g-3 (same buffer) is complete: the buffer is free, and
                         // if that job was the last reader of its K/V tile, the stage is too.
-                        if (!wait_warp(bar(C::kBarPvDone + b), ((g / C::kSBufs) - 1) & 1, wc,
+                        if (!wait_warp_sleep(bar(C::kBarPvDone + b), ((g / C::kSBufs) - 1) & 1, wc,
                                        kRoleMma * 1000 + C::kBarPvDone + b, g)) {
                             ok = false;
                             break;
@@ -265,10 +265,10 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
             }
             // Drain: the last O += P V groups have completed (every S before them has too).
             for (int r = max(0, g - C::kSBufs); r < g && ok; ++r)
-                ok = wait_warp(bar(C::kBarPvDone + r % C::kSBufs), (r / C::kSBufs) & 1, wc,
+                ok = wait_warp_sleep(bar(C::kBarPvDone + r % C::kSBufs), (r / C::kSBufs) & 1, wc,
                                kRoleMma * 1000 + C::kBarPvDone + r % C::kSBufs, r);
             mma_commit_warp(bar(C::kBarDrain + 0));
-            wait_warp(bar(C::kBarDrain + 0), 0, wc, kRoleMma * 1000 + C::kBarDrain, 0, false);
+            wait_warp_sleep(bar(C::kBarDrain + 0), 0, wc, kRoleMma * 1000 + C::kBarDrain, 0, false);
             __syncwarp();
         } else if (warp == C::kWarpStore) {
             // ================================ O store =====================================
@@ -330,9 +330,9 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                         // previous item's O read out: the softmax warpgroup reads it (and
                         // waits for the loads) before it writes the item's first P, so
                         // p_full implies it.
-                        if (!wait_warp(bar(C::kBarPFull + b), (g / C::kSBufs) & 1, wc, kRoleMma * 1000 + C::kBarPFull + b,
+                        if (!wait_warp_sleep(bar(C::kBarPFull + b), (g / C::kSBufs) & 1, wc, kRoleMma * 1000 + C::kBarPFull + b,
                                        g) ||
-                            !wait_warp(bar(C::kBarVFull + s), (Gt / C::kStages) & 1, wc,
+                            !wait_warp_sleep(bar(C::kBarVFull + s), (Gt / C::kStages) & 1, wc,
                                        kRoleMma * 1000 + C::kBarVFull + s, g)) {
                             ok = false;
                             break;
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                     Gb += max(w.n0, w.n1);
                 }
                 mma_commit_warp(bar(C::kBarDrain + 1));
-                wait_warp(bar(C::kBarDrain + 1), 0, wc, kRoleMma * 1000 + C::kBarDrain + 1, 0, false);
+                wait_warp_sleep(bar(C::kBarDrain + 1), 0, wc, kRoleMma * 1000 + C::kBarDrain + 1, 0, false);
             }
             __syncwarp();
         }

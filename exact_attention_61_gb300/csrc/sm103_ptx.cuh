@@ -66,6 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same, allowing the thread to be suspended for up to `hint_ns` nanoseconds while the
+// phase is not complete (it resumes when the phase completes): a waiting warp then
+// spends no issue slots polling.
+template <uint32_t hint_ns>
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Non-blocking test (never suspends the thread): true if the phase has completed.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
