@@ -11,6 +11,14 @@ Timing: W warm-up steps (plus enough extra steps to keep the GPU busy for
 warm-up, then K steps timed with CUDA events on the launching stream, the L2
 cache flushed (a write of twice its size) before every step outside the events,
 a barrier and a synchronize on both sides of the timed region, max over ranks.
+`value`, `ms_per_step` and `roofline.achieved` come from the per-step medians
+(the means, p10 and p90 are reported beside them).
+
+After the timed region, outside it: a second pass of K flushed steps (the run
+repeated, to show its spread), K steps without the L2 flush, the HBM-bound
+points of the sequence sweep, and the end-to-end call from host buffers. The
+cpu_baseline leg times the fp64 oracle on sampled rows and compares those rows
+with the outputs of the last timed launch of each mask.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -43,10 +51,20 @@ DTYPE = "bf16"
 SEED = 61002
 WORKLOAD = "b4h16n4096d64 bf16, non-causal + causal forward per step"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_b4h16n4096d64.md")
-KERNEL_SOURCES = ["exact_attention_61_gb300/csrc/attn_fwd_kernel.cuh",
+KERNEL_SOURCES = ["exact_attention_61_gb300/csrc/attn_fwd_persist.cuh",
+                  "exact_attention_61_gb300/csrc/attn_fwd_kernel.cuh",
                   "exact_attention_61_gb300/csrc/sm103_ptx.cuh",
                   "exact_attention_61_gb300/csrc/attn_internal.h",
                   "exact_attention_61_gb300/csrc/attn_fwd_inst.cu"]
+
+
+# The sequence-sweep points that are bound by HBM rather than by the tensor cores
+# (B = 16384 / N, H = 16, d = 64): short rows leave little compute per byte moved.
+HBM_SWEEP = [(32, 16, 512, 64, False), (32, 16, 512, 64, True), (16, 16, 1024, 64, True)]
+# Tolerances of the parity check (bf16 O, and the LSE in natural-log units).
+TOL_O, TOL_LSE = 3.2e-2, 1e-3
+# ex2 results per SM per clock: 16 on sm_100 parts, doubled on Blackwell Ultra (sm_103).
+EX2_PER_SM_CLK = 32
 
 
 def log(*a):
@@ -64,6 +82,61 @@ def step_flops() -> float:
 
 def tflops(flops: float, ms: float) -> float:
     return flops / (ms * 1e-3) / 1e12
+
+
+def fwd_bytes(B_: int, H_: int, N_: int, d: int, elem: int = 2) -> int:
+    """Algorithmic HBM bytes of one forward: q, k, v read once, o and the fp32 LSE
+    written once."""
+    return 4 * elem * B_ * H_ * N_ * d + 4 * B_ * H_ * N_
+
+
+def softmax_exps(B_: int, H_: int, N_: int, causal: bool) -> int:
+    """Exponentials the softmax takes by definition: one per unmasked score."""
+    per_head = N_ * (N_ + 1) // 2 if causal else N_ * N_
+    return B_ * H_ * per_head
+
+
+def ex2_peak(sms: int, sm_mhz: float) -> float:
+    """Nominal ex2 throughput (results/s) of `sms` SMs at `sm_mhz`."""
+    return EX2_PER_SM_CLK * sms * sm_mhz * 1e6
+
+
+def cpu_model(cpuinfo: str | None = None) -> str:
+    """The host CPU's model from /proc/cpuinfo: the x86 'model name' line, else the
+    Arm implementer and part numbers (named where known)."""
+    if cpuinfo is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                cpuinfo = f.read()
+        except OSError:
+            return "unknown"
+    fields = {}
+    for line in cpuinfo.splitlines():
+        if ":" in line:
+            key, val = line.split(":", 1)
+            fields.setdefault(key.strip().lower(), val.strip())
+    if fields.get("model name"):
+        return fields["model name"]
+    impl, part = fields.get("cpu implementer"), fields.get("cpu part")
+    if impl and part:
+        known = {("0x41", "0xd4f"): "Arm Neoverse-V2", ("0x41", "0xd40"): "Arm Neoverse-V1",
+                 ("0x41", "0xd0c"): "Arm Neoverse-N1", ("0x41", "0xd8e"): "Arm Neoverse-N3",
+                 ("0x41", "0xd84"): "Arm Neoverse-V3"}
+        name = known.get((impl.lower(), part.lower()))
+        return f"{name} (implementer {impl}, part {part})" if name else f"Arm implementer {impl}, part {part}"
+    return "unknown"
+
+
+def spot_check(o_gpu, lse_gpu, o_ref, lse_ref, tol_o: float = TOL_O, tol_lse: float = TOL_LSE) -> dict:
+    """Element-wise comparison of sampled output rows (numpy arrays, [R, d] and [R])."""
+    import numpy as np
+    d_o = np.abs(np.asarray(o_gpu, dtype=np.float64) - o_ref)
+    d_l = np.abs(np.asarray(lse_gpu, dtype=np.float64) - lse_ref)
+    return {"rows": int(d_l.size), "max_abs_err_o": float(d_o.max(initial=0.0)),
+            "max_abs_err_lse": float(d_l.max(initial=0.0)),
+            "over_tol_o": int((d_o > tol_o).sum()), "over_tol_lse": int((d_l > tol_lse).sum()),
+            "tol_o": tol_o, "tol_lse": tol_lse,
+            "ok": bool((d_o <= tol_o).all() and (d_l <= tol_lse).all())}
 
 
 def aggregate(ms_per_rank, flops_per_rank_step: float, world: int) -> dict:
@@ -189,18 +262,21 @@ def _row_flops(rows, causal: bool) -> float:
     return float(sum(4.0 * ((int(r) % N) + 1) * D for r in rows))
 
 
-def oracle_rate(q64, k64, v64, n_rows: int, seed: int = 0):
+def oracle_rate(q64, k64, v64, n_rows: int, seed: int = 0, keep: bool = False):
     """Time the oracle on n_rows sampled query rows under each mask. Returns
-    (FLOPs, seconds)."""
+    (FLOPs, seconds), and with keep=True also (rows, {causal: (O rows, LSE rows)})."""
     import oracle
     rows = _sample_rows(n_rows, seed)
     scale = 1.0 / math.sqrt(D)
     flops = secs = 0.0
+    outs = {}
     for causal in (False, True):
         t0 = time.perf_counter()
-        oracle.attn_fwd_rows(q64, k64, v64, causal, rows, scale)
+        outs[causal] = oracle.attn_fwd_rows(q64, k64, v64, causal, rows, scale)
         secs += time.perf_counter() - t0
         flops += _row_flops(rows, causal)
+    if keep:
+        return flops, secs, rows, outs
     return flops, secs
 
 
@@ -213,15 +289,28 @@ def calibrate_rows(q64, k64, v64, target_s: float) -> int:
         n *= 4
 
 
-def cpu_baseline(q, k, v, target_s: float = 12.0) -> dict:
+def cpu_baseline(q, k, v, target_s: float = 12.0, timed_outputs=None) -> dict:
+    """The fp64 oracle on the host cores over a bounded sample of rows. With
+    `timed_outputs` = {causal: (O [B,H,N,d], LSE [B,H,N]) on the host}, the sampled rows
+    are also compared with those outputs of the timed launches."""
     import oracle
     q64, k64, v64 = oracle.to_f64(q), oracle.to_f64(k), oracle.to_f64(v)
     n = calibrate_rows(q64, k64, v64, target_s)
-    flops, secs = oracle_rate(q64, k64, v64, n, seed=2)
-    return {"value": tflops(flops, secs * 1e3), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{n} random query rows of the B=4,H=16,N=4096,d=64 bf16 problem, "
-                      f"each under both masks, fp64 C oracle; {secs:.1f} s of CPU work"}
+    flops, secs, rows, outs = oracle_rate(q64, k64, v64, n, seed=2, keep=True)
+    res = {"value": tflops(flops, secs * 1e3), "unit": UNIT, "cores": oracle.num_threads(),
+           "cpu_model": cpu_model(), "kind": "oracle",
+           "sample": f"{n} random query rows of the B=4,H=16,N=4096,d=64 bf16 problem, "
+                     f"each under both masks, fp64 C oracle; {secs:.1f} s of CPU work"}
+    if timed_outputs is not None:
+        res["parity_of_timed_outputs"] = {}
+        import torch
+        idx = torch.from_numpy(rows)
+        for causal, (o_h, l_h) in timed_outputs.items():
+            o_rows = o_h.reshape(-1, D)[idx].double().numpy()
+            l_rows = l_h.reshape(-1)[idx].double().numpy()
+            res["parity_of_timed_outputs"]["causal" if causal else "noncausal"] = spot_check(
+                o_rows, l_rows, outs[causal][0], outs[causal][1])
+    return res
 
 
 # ---------------------------------------------------------------------------------------------
@@ -258,7 +347,7 @@ def run_reference(args) -> int:
            "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D,
                       "step": f"{n} sampled query rows x both masks"},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
-                            "kind": "oracle",
+                            "cpu_model": cpu_model(), "kind": "oracle",
                             "sample": f"{n} random query rows per step under both masks, fp64 C oracle"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -287,20 +376,39 @@ def run_ours(args) -> int:
 
     q_h, k_h, v_h = make_qkv(B, H, N, D, DTYPE, SEED)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    # one output pair per mask, so that both timed launches' outputs survive the step
+    o = {c: torch.empty_like(q) for c in (False, True)}
+    lse = {c: torch.empty((B, H, N), dtype=torch.float32, device=dev) for c in (False, True)}
     scale = 1.0 / math.sqrt(D)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
     dt = attn.ATTN_BF16
 
-    def launch(causal):
-        st = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                           B, H, N, D, causal, scale, dt, sptr)
+    def launch(causal, q_=q, k_=k, v_=v, o_=None, l_=None, shape=(B, H, N, D)):
+        o_ = o[causal] if o_ is None else o_
+        l_ = lse[causal] if l_ is None else l_
+        st = attn.attn_fwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), l_.data_ptr(),
+                           *shape, causal, 1.0 / math.sqrt(shape[3]), dt, sptr)
         if st != attn.ATTN_OK:
             raise RuntimeError(f"attn_fwd failed: {attn.strerror(st)}")
+
+    def timed_steps(n, flush_l2=True):
+        """n steps (non-causal then causal launch), per-launch CUDA-event times in ms."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for i in range(n):
+            if flush_l2:
+                flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            launch(False)
+            ev[i][1].record(stream)
+            launch(True)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        return ([ev[i][0].elapsed_time(ev[i][1]) for i in range(n)],
+                [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)])
 
     sampler = ClockSampler(local_rank) if args.clocks else None
     # ---- warm-up: W steps, then keep the GPU busy until --warmup-seconds have passed -----
@@ -316,29 +424,48 @@ def run_ours(args) -> int:
     torch.cuda.synchronize(dev)
     torch.cuda.reset_peak_memory_stats(dev)
 
-    # ---- timed region ------------------------------------------------------------------
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # ---- timed region: exactly K steps --------------------------------------------------
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.time()
     w0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        launch(False)
-        ev[i][1].record(stream)
-        launch(True)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize(dev)
+    t_nc, t_c = timed_steps(args.steps)
     barrier()
     wall_s = time.perf_counter() - w0
     t1 = time.time()
     launches = 2 * args.steps
-    t_nc = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    t_c = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     t_step = [a + b for a, b in zip(t_nc, t_c)]
-    ms_local = statistics.fmean(t_step)
     peak_mem_gb = torch.cuda.max_memory_allocated(dev) / 1e9
+    # outputs of the last timed launch of each mask, for the parity spot check
+    timed_out = {c: (o[c].cpu(), lse[c].cpu()) for c in (False, True)}
+
+    # ---- outside the timed region: the run repeated, and the same steps without the flush --
+    r_nc, r_c = timed_steps(args.steps)
+    n_nc, n_c = timed_steps(args.steps, flush_l2=False)
+    t2 = time.time()
+
+    # ---- the HBM-bound points of the sequence sweep (flushed, outside the timed region) ---
+    sweep = []
+    peaks = measured_peaks()
+    for (b_, h_, n_, d_, causal) in HBM_SWEEP:
+        qs, ks, vs = (t.to(dev) for t in make_qkv(b_, h_, n_, d_, DTYPE, SEED + 7))
+        os_, ls_ = torch.empty_like(qs), torch.empty((b_, h_, n_), dtype=torch.float32, device=dev)
+        ts = []
+        for i in range(max(3, args.warmup) + args.steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(causal, qs, ks, vs, os_, ls_, (b_, h_, n_, d_))
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms_s = statistics.median(a.elapsed_time(b) for a, b in ts[max(3, args.warmup):])
+        by = fwd_bytes(b_, h_, n_, d_)
+        sweep.append({"B": b_, "H": h_, "N": n_, "d": d_, "causal": causal, "ms_median": ms_s,
+                      "tflops": tflops(counts.attn_flops(b_, h_, n_, d_, causal), ms_s),
+                      "algorithmic_bytes": by, "gbs": by / (ms_s * 1e-3) / 1e9,
+                      "hbm_frac": by / (ms_s * 1e-3) / 1e9 / peaks["hbm_gbs"]})
+        del qs, ks, vs, os_, ls_
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region) --
     # attn_fwd_host, once per mask: the first call copies q, k, v from page-locked host
@@ -351,7 +478,7 @@ def run_ours(args) -> int:
     n_chunks, heads_per_chunk = attn.host_plan(B, H, N, D)
     e2e_steps = max(3, min(args.steps, 50))
     h2d = 3 * q_h.numel() * q_h.element_size()
-    d2h = 2 * (o.numel() * o.element_size() + lse.numel() * 4)
+    d2h = 2 * (q.numel() * q.element_size() + B * H * N * 4)
 
     def e2e_step():
         for j, causal in enumerate((False, True)):
@@ -377,16 +504,37 @@ def run_ours(args) -> int:
     if sampler:
         sampler.stop()
 
-    # ---- aggregate over ranks -----------------------------------------------------------
-    ms, e2e_ms, ms_nc, ms_c = allreduce_max(
-        [ms_local, e2e_ms_local, statistics.fmean(t_nc), statistics.fmean(t_c)], world, dev)
+    # ---- aggregate over ranks (medians per rank, max over ranks) ---------------------------
+    med = statistics.median
+    ms, e2e_ms, ms_nc, ms_c = allreduce_max([med(t_step), e2e_ms_local, med(t_nc), med(t_c)], world, dev)
     if rank == 0:
-        peaks = measured_peaks()
         f_nc = counts.attn_flops(B, H, N, D, False)
         f_c = counts.attn_flops(B, H, N, D, True)
         agg = aggregate([ms], f_nc + f_c, world)
         achieved = tflops(f_nc, ms_nc)
         traffic = profiled_traffic()
+        clocks = summarize_clocks(sampler.samples, t0 - args.warmup_seconds, t1) if sampler else None
+        sm_mhz = (clocks or {}).get("sm_mhz") or 0.0
+
+        def kstats(ts, f, causal):
+            m = med(ts)
+            e = softmax_exps(B, H, N, causal)
+            r = {"ms_median": m, "ms_mean": statistics.fmean(ts), "ms_p10": _pct(ts, 10),
+                 "ms_p90": _pct(ts, 90), "tflops": tflops(f, m),
+                 "frac_of_peak": tflops(f, m) / peaks["bf16_tflops"],
+                 "exps_per_s": e / (m * 1e-3)}
+            if sm_mhz:
+                r["exps_frac_of_ex2_peak"] = r["exps_per_s"] / ex2_peak(sms, sm_mhz)
+            return r
+
+        def pass_summary(a_nc, a_c):
+            m_step = med([x + y for x, y in zip(a_nc, a_c)])
+            return {"ms_per_step_median": m_step, "tflops": tflops(f_nc + f_c, m_step),
+                    "noncausal_tflops": tflops(f_nc, med(a_nc)), "causal_tflops": tflops(f_c, med(a_c))}
+
+        rep_pass = pass_summary(r_nc, r_c)
+        rep_pass["diff_vs_timed_pct"] = 100.0 * (rep_pass["ms_per_step_median"] / ms - 1.0)
+        nf_pass = pass_summary(n_nc, n_c)
         out = {
             "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": n_warm, "ms_per_step": ms, "higher_is_better": True,
@@ -394,21 +542,28 @@ def run_ours(args) -> int:
             "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "scale": scale,
                        "causal": [False, True], "seed": SEED,
                        "l2": "flushed before every step (write of 2x L2 size, outside the events)",
+                       "statistic": "median over the timed steps (mean, p10, p90 in per_kernel)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "per_kernel": {
-                "noncausal": {"ms_mean": ms_nc, "ms_median": statistics.median(t_nc),
-                              "ms_p10": _pct(t_nc, 10), "ms_p90": _pct(t_nc, 90),
-                              "tflops": tflops(f_nc, ms_nc), "frac_of_peak": tflops(f_nc, ms_nc) / peaks["bf16_tflops"]},
-                "causal": {"ms_mean": ms_c, "ms_median": statistics.median(t_c),
-                           "ms_p10": _pct(t_c, 10), "ms_p90": _pct(t_c, 90),
-                           "tflops": tflops(f_c, ms_c), "frac_of_peak": tflops(f_c, ms_c) / peaks["bf16_tflops"],
-                           "executed_tflops": tflops(counts.kernel_executed_flops(B, H, N, D, True), ms_c)}},
-            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<64,false,bf16>",
+                "noncausal": kstats(t_nc, f_nc, False),
+                "causal": {**kstats(t_c, f_c, True),
+                           "executed_tflops": tflops(counts.kernel_executed_flops(B, H, N, D, True), med(t_c))}},
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_persist_kernel<non-causal, bf16>",
                          "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                          "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
                          if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16",
-                         "algorithmic_flops_per_launch": f_nc},
+                         "algorithmic_flops_per_launch": f_nc,
+                         "statistic": "median launch time of the timed steps"},
+            "softmax_exps": {"per_step": softmax_exps(B, H, N, False) + softmax_exps(B, H, N, True),
+                             "per_s": (softmax_exps(B, H, N, False) + softmax_exps(B, H, N, True)) / (ms * 1e-3),
+                             "ex2_peak_per_s": ex2_peak(sms, sm_mhz) if sm_mhz else None,
+                             "ex2_peak_basis": f"{EX2_PER_SM_CLK} ex2/clk/SM x {sms} SMs x median SM clock"},
+            "repeat": rep_pass,
+            "no_l2_flush": {**nf_pass, "note": "the same K steps back to back, L2 not flushed"},
+            "hbm_sweep": {"points": sweep, "peak_gbs": peaks["hbm_gbs"],
+                          "note": "the HBM-bound points of the sequence sweep (B=16384/N, H=16, d=64), "
+                                  "algorithmic bytes (q,k,v read, o,lse written once) / median time"},
             "e2e": {"value": tflops((f_nc + f_c) * world, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "call": f"attn_fwd_host per mask, the second on the inputs the first staged "
@@ -416,13 +571,15 @@ def run_ours(args) -> int:
                             f"chunks of {heads_per_chunk} heads)"},
             "gpu_launches": launches,
             "wall_s_timed_region": wall_s,
+            "wall_s_after_timed_region": t2 - t1,
             "peak_mem_gb": peak_mem_gb,
         }
-        if sampler:
-            out["clocks"] = summarize_clocks(sampler.samples, t0 - args.warmup_seconds, t1)
+        if clocks is not None:
+            out["clocks"] = clocks
         if args.cpu_baseline and world == 1:
             log("timing the fp64 oracle on the host cores ...")
-            out["cpu_baseline"] = cpu_baseline(q_h, k_h, v_h, target_s=args.cpu_seconds)
+            out["cpu_baseline"] = cpu_baseline(q_h, k_h, v_h, target_s=args.cpu_seconds,
+                                               timed_outputs=timed_out)
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()

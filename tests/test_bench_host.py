@@ -128,3 +128,39 @@ def test_bwd_flops():
     assert bench.bwd_flops(4, 16, 4096, 64, False) == 2.5 * counts.attn_flops(4, 16, 4096, 64, False)
     assert bench.bwd_flops(4, 16, 4096, 64, True) == 2.5 * counts.attn_flops(4, 16, 4096, 64, True)
     assert bench.parse_args(["--bwd"]).bwd
+
+
+def test_fwd_bytes_and_exps():
+    # q, k, v, o: 4 tensors of B*H*N*d bf16; lse: B*H*N fp32
+    assert bench.fwd_bytes(4, 16, 4096, 64) == 4 * 2 * 4 * 16 * 4096 * 64 + 4 * 4 * 16 * 4096
+    assert bench.softmax_exps(1, 1, 4, False) == 16
+    assert bench.softmax_exps(1, 1, 4, True) == 10          # 1 + 2 + 3 + 4 unmasked scores
+    assert bench.softmax_exps(2, 3, 5, True) == 6 * 15
+    assert bench.ex2_peak(152, 2000.0) == pytest.approx(32 * 152 * 2e9)
+    for b_, h_, n_, d_, causal in bench.HBM_SWEEP:
+        assert b_ * n_ == 16384 and h_ == 16 and d_ == 64
+
+
+def test_cpu_model_parsing():
+    x86 = "processor\t: 0\nvendor_id\t: GenuineIntel\nmodel name\t: Intel(R) Xeon(R) Platinum 8480+\n"
+    assert bench.cpu_model(x86) == "Intel(R) Xeon(R) Platinum 8480+"
+    arm = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\nCPU part\t: 0xd4f\n"
+    assert bench.cpu_model(arm).startswith("Arm Neoverse-V2")
+    odd = "CPU implementer\t: 0x61\nCPU part\t: 0x022\n"
+    assert bench.cpu_model(odd) == "Arm implementer 0x61, part 0x022"
+    assert bench.cpu_model("") == "unknown"
+    assert isinstance(bench.cpu_model(), str)
+
+
+def test_spot_check_flags_errors():
+    import numpy as np
+    rng = np.random.default_rng(0)
+    o_ref, l_ref = rng.standard_normal((8, 64)), rng.standard_normal(8)
+    r = bench.spot_check(o_ref + 0.01, l_ref + 1e-4, o_ref, l_ref)
+    assert r["ok"] and r["rows"] == 8 and r["over_tol_o"] == 0
+    bad = o_ref.copy()
+    bad[3, 5] += 0.05
+    r = bench.spot_check(bad, l_ref, o_ref, l_ref)
+    assert not r["ok"] and r["over_tol_o"] == 1 and r["max_abs_err_o"] == pytest.approx(0.05)
+    r = bench.spot_check(o_ref, l_ref + 2e-3, o_ref, l_ref)
+    assert not r["ok"] and r["over_tol_lse"] == 8

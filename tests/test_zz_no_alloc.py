@@ -56,3 +56,30 @@ def test_oversize_is_rejected(cuda_lib):
     with pytest.raises(cuda_lib.AttnError) as e:
         cuda_lib.fwd_kv_static(q, k, k, o, lse)
     assert e.value.status == cuda_lib.ATTN_ERR_SCRATCH_TOO_SMALL
+
+
+@pytest.mark.gpu
+def test_no_device_memory_is_taken(cuda_lib):
+    """After one warm-up call of each kind (module loading, first use of the scratch),
+    further calls, split or not, leave the device's free memory (cudaMemGetInfo) and
+    torch's allocated bytes unchanged."""
+    cases = [(1, 4, 300, 1000, 64, "bf16", 81),   # split keys: partials in the static scratch
+             (8, 16, 1000, 1000, 64, "bf16", 82),  # no split
+             (2, 3, 16, 5000, 128, "fp16", 83)]    # split, d = 128
+    bufs = []
+    for B, H, Nq, Nk, d, dtype, seed in cases:
+        q, k, v = (t.cuda() for t in make_qkv_kv(B, H, Nq, Nk, d, dtype, seed))
+        bufs.append((q, k, v, torch.empty_like(q), torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")))
+    for mask in ("none", "causal_bottom_right"):
+        for q, k, v, o, lse in bufs:
+            cuda_lib.fwd_kv_static(q, k, v, o, lse, mask=mask)
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for _ in range(3):
+        for mask in ("none", "causal_bottom_right"):
+            for q, k, v, o, lse in bufs:
+                cuda_lib.fwd_kv_static(q, k, v, o, lse, mask=mask)
+    torch.cuda.synchronize()
+    free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    assert alloc1 == alloc0, f"torch allocated {alloc1 - alloc0} bytes"
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
