@@ -129,6 +129,9 @@ def load(path: str = LIB_PATH):
             lib.attn_probe_plan_split.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_size_t, ctypes.c_int64,
                                                                         ctypes.POINTER(ctypes.c_int64)]
             lib.attn_probe_plan_split.restype = ctypes.c_int
+            lib.attn_probe_plan_decode.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_size_t, ctypes.c_int64,
+                                                                          ctypes.POINTER(ctypes.c_int64)]
+            lib.attn_probe_plan_decode.restype = ctypes.c_int
             lib.attn_probe_plan_host.argtypes = [ctypes.c_int64] * 3 + [ctypes.POINTER(ctypes.c_int64)]
             lib.attn_probe_plan_host.restype = ctypes.c_int64
             _lib = lib
@@ -202,6 +205,16 @@ def plan_split_for(BH, Nq, Nk, d, ws_bytes, sms) -> Tuple[int, int, int]:
     if st != ATTN_OK:
         raise AttnError(st, f"attn_probe_plan_split: {strerror(st)}")
     return int(out[0]), int(out[1]), int(out[2])
+
+
+def plan_decode_for(BH, Nq, Nk, d, ws_bytes, sms) -> Tuple[int, int, int, int]:
+    """(key ranges per head, keys per range, CTAs, workspace bytes) of the streaming
+    decode kernel on a GPU with `sms` SMs (test hook)."""
+    out = (ctypes.c_int64 * 4)()
+    st = load().attn_probe_plan_decode(BH, Nq, Nk, d, ws_bytes, sms, out)
+    if st != ATTN_OK:
+        raise AttnError(st, f"attn_probe_plan_decode: {strerror(st)}")
+    return int(out[0]), int(out[1]), int(out[2]), int(out[3])
 
 
 def plan_host_for(BH, N, sms) -> Tuple[int, int]:

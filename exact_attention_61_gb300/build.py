@@ -6,6 +6,7 @@ with the CUDA runtime linked statically):
   attn_static_scratch.cu             device scratch of attn_fwd_kv_static (own module)
   probe.cu                           one-tile tensor-core probe (test hook)
   attn_merge.cu                      merge of split-key partials
+  attn_decode.cu                     streaming decode kernel (up to 4 query rows)
   attn_fwd_inst.cu x 4               forward kernel, one unit per (d, dtype)
   attn_bwd_aux.cu                    backward prologue (D, lse2) and dQ cast
   attn_bwd_inst.cu x 4               backward kernel, one unit per (d, dtype)
@@ -34,6 +35,7 @@ UNITS = [
     ("attn_static_scratch.cu", [], "attn_static_scratch.o"),
     ("probe.cu", [], "probe.o"),
     ("attn_merge.cu", [], "attn_merge.o"),
+    ("attn_decode.cu", [], "attn_decode.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=0"], "attn_fwd_d64_f16.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=64", "-DATTN_INST_BF16=1"], "attn_fwd_d64_bf16.o"),
     ("attn_fwd_inst.cu", ["-DATTN_INST_D=128", "-DATTN_INST_BF16=0"], "attn_fwd_d128_f16.o"),

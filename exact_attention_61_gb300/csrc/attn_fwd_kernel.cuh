@@ -681,28 +681,54 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
 // Merge of split partials: per (b, h, query row), with log2-sum-exp values x_s of the
 // splits, X = max_s x_s, w_s = 2^(x_s - X), O = sum_s w_s O_s / sum_s w_s and
-// LSE = (X + log2 sum_s w_s) ln 2. One warp per row; lanes cover the head dimension.
+// LSE = (X + log2 sum_s w_s) ln 2. One warp per row: the lanes share out the splits for X
+// and the weights, then cover the head dimension while the splits' O_s are summed.
 template <bool BF16>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const MergeParams p) {
     const int warp_global = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31u);
     if (warp_global >= p.BH * p.Nq) return;
     const int bh = warp_global / p.Nq, i = warp_global % p.Nq;
-    const float* lp = p.lse_part + static_cast<size_t>(bh) * p.n_splits * p.Nq + i;
+    const int S = p.n_splits;
+    const float* lp = p.lse_part + static_cast<size_t>(bh) * S * p.Nq + i;
+    // X = max_s x_s, the lanes over the ranges
     float X = -INFINITY;
-    for (int s = 0; s < p.n_splits; ++s) X = fmaxf(X, lp[static_cast<size_t>(s) * p.Nq]);
+    for (int s = lane; s < S; s += 32) X = fmaxf(X, lp[static_cast<size_t>(s) * p.Nq]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) X = fmaxf(X, __shfl_xor_sync(0xffffffffu, X, off));
     const int per_lane = p.d / 32;  // 2 or 4
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float wsum = 0.f;
     if (X != -INFINITY) {
-        for (int s = 0; s < p.n_splits; ++s) {
-            const float x = lp[static_cast<size_t>(s) * p.Nq];
-            if (x == -INFINITY) continue;
-            const float w = ex2_ftz(x - X);
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            // w_s = 2^(x_s - X) of range s0 + lane (0 for a range without keys), then each
+            // range's O_s weighted in turn, its weight broadcast; empty ranges are skipped,
+            // so their partial outputs are never read
+            const int s = s0 + lane;
+            const float x = s < S ? lp[static_cast<size_t>(s) * p.Nq] : -INFINITY;
+            const float w = x == -INFINITY ? 0.f : ex2_ftz(x - X);
             wsum += w;
-            const float* op = p.o_part + ((static_cast<size_t>(bh) * p.n_splits + s) * p.Nq + i) * p.d;
-            for (int e = 0; e < per_lane; ++e) acc[e] += w * op[lane * per_lane + e];
+            const int nb = min(32, S - s0);
+#pragma unroll 4
+            for (int j = 0; j < nb; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+                if (wj == 0.f) continue;
+                const float* op = p.o_part + ((static_cast<size_t>(bh) * S + s0 + j) * p.Nq + i) * p.d + lane * per_lane;
+                if (per_lane == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(op);
+                    acc[0] += wj * v.x;
+                    acc[1] += wj * v.y;
+                    acc[2] += wj * v.z;
+                    acc[3] += wj * v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(op);
+                    acc[0] += wj * v.x;
+                    acc[1] += wj * v.y;
+                }
+            }
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     const size_t orow = (static_cast<size_t>(bh) * p.Nq + i) * p.d + lane * per_lane;

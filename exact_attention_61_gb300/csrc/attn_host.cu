@@ -217,6 +217,47 @@ SplitPlan plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_by
     return pl;
 }
 
+// Ranges of the keys for the streaming decode kernel: each (head, range) unit is one warp's
+// work, units go round-robin over every warp of a one-CTA-per-SM grid. The number of
+// ranges per head S minimises the slowest warp's work, ceil(BH * S / warps) units of
+// (tiles per range + 1) tile times, the 1 standing for a unit's start and its partial
+// output. Limited by the workspace (S = 1: no workspace, the kernel writes O directly).
+DecodePlan plan_decode(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms) {
+    sms = std::max<int64_t>(sms, 1);
+    const int64_t warps = sms * decode_warps(d, Nq);
+    const int64_t tile = decode_tile_keys(d, Nq);
+    const int64_t n_t = (Nk + tile - 1) / tile;  // tiles per head
+    const uint64_t per_range = static_cast<uint64_t>(BH) * Nq * (d + 1) * 4u;
+    const int64_t fit = static_cast<int64_t>(ws_bytes / per_range);
+    // at most 4096 ranges, and fewer than 2^30 units (the kernel indexes them in int)
+    const int64_t lim = std::min<int64_t>(std::min<int64_t>(std::min<int64_t>(n_t, fit), 4096),
+                                          (int64_t(1) << 30) / std::max<int64_t>(BH, 1));
+    auto cost = [&](int64_t tpr) {
+        const int64_t ranges = (n_t + tpr - 1) / tpr;
+        return ((BH * ranges + warps - 1) / warps) * (tpr + 1);
+    };
+    int64_t best_tpr = n_t;
+    int64_t best = cost(n_t);
+    for (int64_t c = 2; c <= lim; ++c) {
+        const int64_t tpr = (n_t + c - 1) / c;
+        const int64_t k = cost(tpr);
+        if (k < best) {
+            best = k;
+            best_tpr = tpr;
+        }
+    }
+    DecodePlan pl{};
+    pl.range_keys = best_tpr * tile;
+    pl.n_ranges = (Nk + pl.range_keys - 1) / pl.range_keys;
+    const int64_t units = BH * pl.n_ranges;
+    pl.grid = std::min<int64_t>(sms, (units + decode_warps(d, Nq) - 1) / decode_warps(d, Nq));
+    if (pl.n_ranges > 1) {
+        pl.o_part_bytes = static_cast<uint64_t>(BH) * pl.n_ranges * Nq * d * 4u;
+        pl.bytes = pl.o_part_bytes + static_cast<uint64_t>(BH) * pl.n_ranges * Nq * 4u;
+    }
+    return pl;
+}
+
 namespace {
 
 // Which keys a row sees, beyond j < (valid keys of its batch element).
@@ -248,6 +289,38 @@ int fwd_core(const void* q, const void* k, const void* v, void* o, float* lse, i
     const int64_t BH = B * H;
     const int64_t sms = device_sm_count(dev);
     if (sms < 1) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Padding or a window other than the plain causal mask needs the extended instances.
+    const bool x = ms.kv_lens != nullptr || ms.win_left >= 0 || ms.win_right != 0;
+    if (fwd_uses_decode(Nq, x)) {
+        const DecodePlan dp = plan_decode(BH, Nq, Nk, d, ws ? ws_bytes : 0, sms);
+        DecodeParams p{};
+        p.q = q;
+        p.k = k;
+        p.v = v;
+        p.o = o;
+        p.lse = lse;
+        p.err = status;
+        p.BH = static_cast<int>(BH);
+        p.Nq = static_cast<int>(Nq);
+        p.Nk = static_cast<int>(Nk);
+        p.n_ranges = static_cast<int>(dp.n_ranges);
+        p.range_keys = static_cast<int>(dp.range_keys);
+        p.causal = ms.causal ? 1 : 0;
+        p.align_br = ms.align_br;
+        p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+        const bool dsplit = dp.n_ranges > 1;
+        p.o_part = dsplit ? static_cast<float*>(ws) : nullptr;
+        p.lse_part = dsplit ? reinterpret_cast<float*>(static_cast<char*>(ws) + dp.o_part_bytes) : nullptr;
+        e = launch_decode(d, dtype == ATTN_BF16, p, dp.grid, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (dsplit) {
+            MergeParams mp{p.o_part, p.lse_part, o, lse, p.BH, p.Nq, static_cast<int>(d), p.n_ranges};
+            e = launch_merge(dtype == ATTN_BF16, mp, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        return ATTN_OK;
+    }
     const SplitPlan plan = plan_split(BH, Nq, Nk, d, ws ? ws_bytes : 0, sms);
     alignas(64) CUtensorMap maps[4];
     const void* ptrs[4] = {q, k, v, o};
@@ -277,10 +350,7 @@ int fwd_core(const void* q, const void* k, const void* v, void* o, float* lse, i
     const bool split = plan.n_splits > 1;
     p.o_part = split ? static_cast<float*>(ws) : nullptr;
     p.lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.o_part_bytes) : nullptr;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool c = ms.causal;
-    // Padding or a window other than the plain causal mask needs the extended instances.
-    const bool x = ms.kv_lens != nullptr || ms.win_left >= 0 || ms.win_right != 0;
     if (d == 64)
         e = dtype == ATTN_BF16 ? launch_fwd_d64_bf16(c, split, x, maps, p, s)
                                : launch_fwd_d64_f16(c, split, x, maps, p, s);
@@ -803,7 +873,12 @@ int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float
 size_t attn_fwd_kv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d) {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
     if (B > INT32_MAX || H > INT32_MAX || Nq > INT32_MAX || Nk > INT32_MAX || B * H > INT32_MAX) return 0;
-    return static_cast<size_t>(plan_split(B * H, Nq, Nk, d, SIZE_MAX, current_sm_count()).bytes);
+    const int64_t sms = current_sm_count();
+    // A call with at most kDecodeMaxRows rows runs the decode kernel unless it has padding
+    // or a window (attn_fwd_window shares this query): room for either plan.
+    uint64_t bytes = plan_split(B * H, Nq, Nk, d, SIZE_MAX, sms).bytes;
+    if (Nq <= kDecodeMaxRows) bytes = std::max(bytes, plan_decode(B * H, Nq, Nk, d, SIZE_MAX, sms).bytes);
+    return static_cast<size_t>(bytes);
 }
 
 int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
@@ -968,6 +1043,19 @@ int attn_probe_plan_split(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t 
     out[0] = pl.n_splits;
     out[1] = pl.tiles_per_split;
     out[2] = static_cast<int64_t>(pl.bytes);
+    return ATTN_OK;
+}
+
+int attn_probe_plan_decode(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms,
+                           int64_t out[4]) {
+    if (!out || BH < 1 || BH > INT32_MAX || Nq < 1 || Nq > kDecodeMaxRows || Nk < 1 || Nk > INT32_MAX ||
+        (d != 64 && d != 128) || sms < 1)
+        return ATTN_ERR_INVALID_ARG;
+    const DecodePlan pl = plan_decode(BH, Nq, Nk, d, ws_bytes, sms);
+    out[0] = pl.n_ranges;
+    out[1] = pl.range_keys;
+    out[2] = pl.grid;
+    out[3] = static_cast<int64_t>(pl.bytes);
     return ATTN_OK;
 }
 

@@ -56,6 +56,45 @@ cudaError_t launch_fwd_d128_bf16(bool causal, bool split, bool ext, const CUtens
                                cudaStream_t s);
 cudaError_t launch_merge(bool bf16, const MergeParams& p, cudaStream_t s);
 
+// Streaming decode (attn_decode.cu): up to kDecodeMaxRows query rows against a long key
+// sequence, masks none / causal in either alignment (no padding or window), on the CUDA
+// cores: each warp streams K and V tiles of decode_tile_keys keys through its own ring of
+// 1-D bulk copies and keeps the online softmax in fp32. The keys of a head are cut into
+// n_ranges ranges of range_keys keys (a multiple of the tile); with n_ranges > 1 each
+// range writes fp32 O/l and its log2-sum-exp to the split partials of MergeParams' layout
+// ([BH][S][Nq][d], then [BH][S][Nq]) for launch_merge, with n_ranges = 1 the final O and
+// LSE directly.
+constexpr int kDecodeMaxRows = 4;
+inline bool fwd_uses_decode(int64_t Nq, bool ext) { return Nq <= kDecodeMaxRows && !ext; }
+
+struct DecodeParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;           // [BH][Nq][d] dtype, when n_ranges == 1
+    float* lse;        // [BH][Nq], natural log, when n_ranges == 1
+    float* o_part;     // split partials, when n_ranges > 1
+    float* lse_part;
+    uint32_t* err;     // device status record
+    int BH, Nq, Nk;
+    int n_ranges, range_keys;
+    int causal, align_br;  // align_br: diagonal of row i is i + Nk - Nq (else i)
+    float qk_scale;        // scale * log2(e)
+};
+
+struct DecodePlan {
+    int64_t n_ranges, range_keys, grid;
+    uint64_t o_part_bytes, bytes;  // workspace as in SplitPlan (0 when n_ranges == 1)
+};
+// Keys per K/V tile and warps per CTA of the decode kernel (one CTA per SM, 192 KB of
+// shared memory at most) for head dimension d and Nq query rows: 32-key tiles (copies of
+// 8 or 16 KB) where the registers allow a warp per SMSP or more, 16-key tiles to fit
+// three warps per SMSP for several rows at d = 64.
+constexpr int decode_tile_keys(int64_t d, int64_t nq) { return d == 64 && nq > 1 ? 16 : 32; }
+constexpr int decode_warps(int64_t d, int64_t nq) { return d == 128 ? 4 : (nq == 1 ? 8 : 12); }
+DecodePlan plan_decode(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms);
+cudaError_t launch_decode(int64_t d, bool bf16, const DecodeParams& p, int64_t grid, cudaStream_t s);
+
 // How the keys are split over CTAs (n_splits = 1: no split, no workspace).
 struct SplitPlan {
     int64_t n_splits, tiles_per_split;

@@ -127,6 +127,14 @@ int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float
  *    as above, with Nq and Nk in place of N.
  *  - mask: an attn_mask_t; anything else is ATTN_ERR_INVALID_ARG. A row that
  *    sees no key (bottom-right with Nq > Nk) gets O = 0 and LSE = -inf.
+ *  - Nq <= 4: a streaming kernel on the CUDA cores runs instead of the tensor-core
+ *    kernel (a decode step reads each K and V byte for at most four rows, so the
+ *    call is bound by HBM). Each warp streams K and V tiles of 16 keys with bulk
+ *    copies and keeps P and every sum in fp32. Its keys are cut into ranges as a
+ *    balance model of the grid's warps favours; with a workspace, the ranges'
+ *    fp32 partial outputs go there and a second kernel merges them, and with
+ *    none (or too little for two ranges) each head is one range, written
+ *    directly.
  *  - workspace: optional DEVICE scratch owned by the caller (16-byte aligned,
  *    not overlapping the other arrays; NULL or 0 bytes allowed). When the
  *    query rows alone give too few CTAs for the GPU (fewer than two per SM),
@@ -156,7 +164,8 @@ int attn_fwd_kv_checked(const void* q, const void* k, const void* v, void* o, fl
 
 /* attn_fwd_kv_workspace_bytes -- the workspace size with which attn_fwd_kv uses
  * its full split of the keys for these sizes on the current device (0: it never
- * splits them). The split depends on the GPU's SM count, which this looks up once
+ * splits them); for Nq <= 4 the larger of the decode kernel's plan and the
+ * tensor-core split's (attn_fwd_window shares this query and runs the latter). The split depends on the GPU's SM count, which this looks up once
  * per device (a GB300's 152 without a device); otherwise host arithmetic. A
  * smaller workspace is never wrong: the call then splits the keys less. 0 for
  * sizes attn_fwd_kv rejects. */
@@ -272,11 +281,11 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
  * (16777216 bytes) inside this library. The
  * pages have no counterpart; it exists for callers that must not allocate or
  * pass device scratch on the call path.
- *  - Arguments, masks and results as attn_fwd_kv. Sizes whose full split of
- *    the keys needs more than the scratch (attn_fwd_kv_workspace_bytes(...) >
- *    16777216) are rejected with ATTN_ERR_SCRATCH_TOO_SMALL before anything is
- *    enqueued. On GPUs of up to 200 SMs (a GB300 has 152) every size with
- *    Nq <= 16 fits.
+ *  - Arguments, masks and results as attn_fwd_kv. Sizes whose full tensor-core
+ *    split of the keys needs more than the scratch are rejected with
+ *    ATTN_ERR_SCRATCH_TOO_SMALL before anything is enqueued. On GPUs of up to
+ *    200 SMs (a GB300 has 152) every size with Nq <= 16 fits. With Nq <= 4 the
+ *    decode kernel runs with as many key ranges as the scratch holds.
  *  - Nothing in the scratch needs to start at zero: each call writes every
  *    partial it reads before reading it.
  *  - No device or host memory is allocated (no cudaMalloc/cudaFree, no

@@ -123,9 +123,11 @@ def test_kv_host_validation(lib, kw, status):
 
 
 def _splits(attn, B, H, Nq, Nk, d):
-    n = attn.workspace_bytes(B, H, Nq, Nk, d)
+    """Key ranges of the tensor-core split (0: none), from its workspace bytes."""
+    n = attn.plan_split_for(B * H, Nq, Nk, d, 1 << 40, 152)[2]
     per = B * H * Nq * (d + 1) * 4
     assert n % per == 0
+    assert n <= attn.workspace_bytes(B, H, Nq, Nk, d)
     return n // per
 
 
@@ -342,7 +344,8 @@ def test_planners_follow_the_sm_count(lib):
     full = 1 << 40
     n152, tps152, b152 = attn.plan_split_for(256, 1, 8192, 128, full, 152)
     assert n152 == 4 and tps152 == 16 and b152 == 256 * 4 * 1 * 129 * 4
-    assert b152 == attn.workspace_bytes(8, 32, 1, 8192, 128)
+    # (one query row: the streaming decode kernel runs; the query leaves room for both plans)
+    assert b152 <= attn.workspace_bytes(8, 32, 1, 8192, 128)
     assert attn.plan_split_for(256, 1, 8192, 128, full, 76)[0] == 1   # 256 CTAs already fill 76 SMs twice
     # 304 SMs hold the 256 CTAs in one wave (no split); 2048 SMs make room for more ranges
     assert attn.plan_split_for(256, 1, 8192, 128, full, 304)[0] == 1
@@ -357,3 +360,30 @@ def test_planners_follow_the_sm_count(lib):
             assert nbytes == (0 if n == 1 else BH * n * Nq * 65 * 4)
             if Nq <= 16:
                 assert nbytes <= attn.STATIC_SCRATCH_BYTES
+
+
+def test_decode_planner(lib):
+    """The streaming decode kernel's plan: key ranges of whole tiles (32 keys; 16 for
+    several rows at d = 64) covering every key, the workspace the partials need (none for one range), at most one CTA per SM,
+    capped by the workspace, and the plans of the three decode workloads on 152 SMs."""
+    from exact_attention_61_gb300 import attn
+    full = 1 << 40
+    # (BH, Nq, Nk, d) -> (ranges, keys per range)
+    assert attn.plan_decode_for(256, 1, 8192, 128, full, 152)[:2] == (7, 1184)
+    assert attn.plan_decode_for(16, 1, 65536, 128, full, 152)[:2] == (38, 1728)
+    assert attn.plan_decode_for(256, 4, 4096, 64, full, 152)[:2] == (7, 592)
+    for sms in (1, 16, 132, 148, 152, 200):
+        for BH, Nq, Nk, d in ((1, 1, 1, 64), (1, 1, 65536, 128), (256, 4, 4096, 64), (300, 3, 1 << 20, 64),
+                              (5, 2, 777, 128), (4096, 1, 100, 128)):
+            n, rk, grid, nbytes = attn.plan_decode_for(BH, Nq, Nk, d, full, sms)
+            assert rk % (16 if d == 64 and Nq > 1 else 32) == 0 and rk * (n - 1) < Nk <= rk * n
+            assert nbytes == (0 if n == 1 else BH * n * Nq * (d + 1) * 4)
+            warps = 4 if d == 128 else (8 if Nq == 1 else 12)
+            assert 1 <= grid <= sms and grid == min(sms, -(-BH * n // warps))
+            assert nbytes <= attn.workspace_bytes(1, BH, Nq, Nk, d) or sms != 152
+    # the workspace caps the ranges; no workspace: one range, O written directly
+    cap = 3 * 256 * 129 * 4
+    assert attn.plan_decode_for(256, 1, 8192, 128, cap, 152)[0] <= 3
+    assert attn.plan_decode_for(256, 1, 8192, 128, 0, 152)[0::3] == (1, 0)
+    with pytest.raises(attn.AttnError):
+        attn.plan_decode_for(2, 5, 100, 64, full, 152)  # more rows than the decode kernel takes
