@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1) attn_decode_kernel
         pvalid = p_seek();
     };
     for (int i = 0; i < C::kStages; ++i) p_issue_next();
+    griddep_launch_dependents();  // the merge may start launching (it waits for this grid)
 
     // ---- consumer ------------------------------------------------------------------------
     const char* qg = static_cast<const char*>(p.q);

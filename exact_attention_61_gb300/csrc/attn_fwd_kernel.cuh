@@ -681,54 +681,71 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
 // Merge of split partials: per (b, h, query row), with log2-sum-exp values x_s of the
 // splits, X = max_s x_s, w_s = 2^(x_s - X), O = sum_s w_s O_s / sum_s w_s and
-// LSE = (X + log2 sum_s w_s) ln 2. One warp per row: the lanes share out the splits for X
-// and the weights, then cover the head dimension while the splits' O_s are summed.
+// LSE = (X + log2 sum_s w_s) ln 2. One CTA of kMergeWarps warps per row: the threads share
+// out the splits for X; each warp sums the weighted O_s of every kMergeWarps-th split with
+// its lanes over the head dimension; the warps' sums are added in shared memory. Splits
+// without keys (x_s = -inf) are skipped, so their partial outputs are never read. Launched
+// as a dependent of the kernel that wrote the partials, it waits for that kernel first.
+constexpr int kMergeWarps = 8;
+
 template <bool BF16>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const MergeParams p) {
-    const int warp_global = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const MergeParams p) {
+    griddep_wait();
+    __shared__ float red[kMergeWarps][129];
+    const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31u);
-    if (warp_global >= p.BH * p.Nq) return;
-    const int bh = warp_global / p.Nq, i = warp_global % p.Nq;
+    const int row = static_cast<int>(blockIdx.x);
+    const int bh = row / p.Nq, i = row % p.Nq;
     const int S = p.n_splits;
     const float* lp = p.lse_part + static_cast<size_t>(bh) * S * p.Nq + i;
-    // X = max_s x_s, the lanes over the ranges
+    // X = max_s x_s over all threads
     float X = -INFINITY;
-    for (int s = lane; s < S; s += 32) X = fmaxf(X, lp[static_cast<size_t>(s) * p.Nq]);
+    for (int s = static_cast<int>(threadIdx.x); s < S; s += kMergeWarps * 32)
+        X = fmaxf(X, lp[static_cast<size_t>(s) * p.Nq]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) X = fmaxf(X, __shfl_xor_sync(0xffffffffu, X, off));
+    if (lane == 0) red[warp][128] = X;
+    __syncthreads();
+    X = red[0][128];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) X = fmaxf(X, red[w][128]);
+    __syncthreads();
     const int per_lane = p.d / 32;  // 2 or 4
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float wsum = 0.f;
+    float wsum = 0.f;  // this warp's splits (the same value in every lane)
     if (X != -INFINITY) {
-        for (int s0 = 0; s0 < S; s0 += 32) {
-            // w_s = 2^(x_s - X) of range s0 + lane (0 for a range without keys), then each
-            // range's O_s weighted in turn, its weight broadcast; empty ranges are skipped,
-            // so their partial outputs are never read
-            const int s = s0 + lane;
-            const float x = s < S ? lp[static_cast<size_t>(s) * p.Nq] : -INFINITY;
-            const float w = x == -INFINITY ? 0.f : ex2_ftz(x - X);
+#pragma unroll 2
+        for (int s = warp; s < S; s += kMergeWarps) {
+            const float x = lp[static_cast<size_t>(s) * p.Nq];
+            if (x == -INFINITY) continue;
+            const float w = ex2_ftz(x - X);
             wsum += w;
-            const int nb = min(32, S - s0);
-#pragma unroll 4
-            for (int j = 0; j < nb; ++j) {
-                const float wj = __shfl_sync(0xffffffffu, w, j);
-                if (wj == 0.f) continue;
-                const float* op = p.o_part + ((static_cast<size_t>(bh) * S + s0 + j) * p.Nq + i) * p.d + lane * per_lane;
-                if (per_lane == 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(op);
-                    acc[0] += wj * v.x;
-                    acc[1] += wj * v.y;
-                    acc[2] += wj * v.z;
-                    acc[3] += wj * v.w;
-                } else {
-                    const float2 v = *reinterpret_cast<const float2*>(op);
-                    acc[0] += wj * v.x;
-                    acc[1] += wj * v.y;
-                }
+            const float* op = p.o_part + ((static_cast<size_t>(bh) * S + s) * p.Nq + i) * p.d + lane * per_lane;
+            if (per_lane == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(op);
+                acc[0] += w * v.x;
+                acc[1] += w * v.y;
+                acc[2] += w * v.z;
+                acc[3] += w * v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(op);
+                acc[0] += w * v.x;
+                acc[1] += w * v.y;
             }
         }
+    }
+    for (int e = 0; e < per_lane; ++e) red[warp][lane * per_lane + e] = acc[e];
+    if (lane == 0) red[warp][128] = wsum;
+    __syncthreads();
+    if (warp != 0) return;
+    wsum = 0.f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    for (int w = 0; w < kMergeWarps; ++w) wsum += red[w][128];
+    for (int e = 0; e < per_lane; ++e) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) a += red[w][lane * per_lane + e];
+        acc[e] = a;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     const size_t orow = (static_cast<size_t>(bh) * p.Nq + i) * p.d + lane * per_lane;

@@ -238,13 +238,17 @@ DecodePlan plan_decode(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_
     };
     int64_t best_tpr = n_t;
     int64_t best = cost(n_t);
-    for (int64_t c = 2; c <= lim; ++c) {
+    // every c <= lim gives tpr = ceil(n_t / c); visit each distinct tpr once, largest first
+    // (the next c with a smaller tpr is ceil(n_t / (tpr - 1)))
+    for (int64_t c = 2; c <= lim;) {
         const int64_t tpr = (n_t + c - 1) / c;
         const int64_t k = cost(tpr);
         if (k < best) {
             best = k;
             best_tpr = tpr;
         }
+        if (tpr <= 1) break;
+        c = (n_t + tpr - 2) / (tpr - 1);
     }
     DecodePlan pl{};
     pl.range_keys = best_tpr * tile;

@@ -134,6 +134,15 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32
                  : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start before the kernel ahead of it on the stream has finished; griddep_wait blocks
+// until that kernel has completed and its memory operations are visible (a no-op when the
+// launch was ordinary). griddep_launch_dependents lets the next such kernel start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Global -> shared plain bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned), completing transaction bytes on `bar`, with an L2 cache policy.
 __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
