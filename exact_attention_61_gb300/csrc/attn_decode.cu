@@ -9,16 +9,21 @@
 // on the CUDA cores and is laid out for streaming:
 //  - every warp works alone on units (head, range of keys), units assigned round-robin
 //    over all warps of the grid (one CTA per SM; the host's plan picks the ranges);
-//  - lane 0 of a warp streams the unit's K and V tiles (16 or 32 keys; a head's keys are
+//  - lane 0 of a warp streams the unit's K and V tiles (32 keys; a head's keys are
 //    contiguous, so one 1-D bulk copy per tile and tensor) through the warp's own
-//    three-stage ring, with an evict-first L2 policy; the ring runs across units;
+//    two- or three-stage ring, with an evict-first L2 policy; the ring runs across units;
 //  - each key row is read as 16-byte chunks by CH = d/8 consecutive lanes (one chunk per
 //    lane), so a warp reads G = 32/CH whole rows per shared-memory load, conflict-free;
 //    a lane keeps its chunk of each query row (times scale * log2 e) in registers, and the
 //    partial dot products are summed over the CH lanes by shuffles;
 //  - the softmax state (running max m, sum l) is per row and shared by the warp; each
 //    lane accumulates O for its 8 head dimensions over the keys its lane group read.
-//    The groups' l and O are summed at the end of the unit.
+//    The groups' l and O are summed at the end of the unit. Rescaling is lazy, as in the
+//    forward: a row keeps its maximum until a tile's exceeds it by more than kRescaleTau
+//    (log2 units), so O and l are rescaled only then (P stays below 2^8 in fp32);
+//  - with several rows, the dot products of the CH lanes of a key row are summed by a
+//    transposed reduction that leaves one row's score per lane, so the softmax runs once
+//    per lane and key; P of every row is then fetched from its lane for O += P V.
 // A unit writes O / l and its log2-sum-exp to the split partials (merged by
 // attn_merge_kernel), or, with one range per head, the final O and LSE.
 #include <atomic>
@@ -36,7 +41,7 @@ struct DecCfg {
     static constexpr int kWarps = decode_warps(D, NQ);
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int T = decode_tile_keys(D, NQ);
-    static constexpr int kStages = 3;
+    static constexpr int kStages = decode_stages(D, NQ);
     static constexpr int kTileBytes = T * D * 2;        // one K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;  // K, then V
     static constexpr int kWarpBytes = kStages * kStageBytes;
@@ -90,9 +95,21 @@ __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1) attn_decode_kernel
         if (p.causal) e = p.align_br ? r + p.Nk - p.Nq + 1 : r + 1;
         lim[r] = r < p.Nq ? max(0, min(p.Nk, e)) : 0;
     }
-    int vis = 0;  // keys any row sees
+    int vis = 0;       // keys any row sees
+    int lim_min = vis;  // keys every real row sees
 #pragma unroll
     for (int r = 0; r < NQ; ++r) vis = max(vis, lim[r]);
+    lim_min = vis;
+#pragma unroll
+    for (int r = 0; r < NQ; ++r)
+        if (r < p.Nq) lim_min = min(lim_min, lim[r]);
+    // With NQ = 4 the score of one query row ends in each lane after the reduction over
+    // the CH lanes of a key row: row rho = 2 * bit2 + bit1 of the lane (bit 0, and bit 3
+    // for CH = 16, hold copies); src(r) is the first lane of the group holding row r.
+    const int rho = ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+    const int lim_rho = lim[rho < NQ ? rho : 0];
+    const int gbase = lane & ~(C::CH - 1);
+    auto src = [&](int r) { return gbase + ((r >> 1) << 2) + ((r & 1) << 1); };
 
     const int W = static_cast<int>(gridDim.x) * C::kWarps;
     const int gw = static_cast<int>(blockIdx.x) * C::kWarps + warp;
@@ -110,10 +127,11 @@ __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1) attn_decode_kernel
     const char* kg = static_cast<const char*>(p.k);
     const char* vg = static_cast<const char*>(p.v);
     int pu = gw, pt = 0, pnt = 0, pbh = 0, pkb = 0, pke = 0;
+    // first unit with tiles at or after pu (pt = 0)
     auto p_seek = [&]() -> bool {
-        for (; pu < U; pu += W, pt = 0) {
+        for (; pu < U; pu += W) {
             pnt = unit_tiles(pu, pbh, pkb, pke);
-            if (pt < pnt) return true;
+            if (pnt > 0) return true;
         }
         return false;
     };
@@ -132,8 +150,11 @@ __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1) attn_decode_kernel
             bulk_load_hint(wbase + s * C::kStageBytes + C::kTileBytes, vg + off, bytes, bar(s), pol);
         }
         ++n_issued;
-        ++pt;
-        pvalid = p_seek();
+        if (++pt == pnt) {
+            pt = 0;
+            pu += W;
+            pvalid = p_seek();
+        }
     };
     for (int i = 0; i < C::kStages; ++i) p_issue_next();
     griddep_launch_dependents();  // the merge may start launching (it waits for this grid)
@@ -174,60 +195,134 @@ __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1) attn_decode_kernel
             const uint8_t* sv = sk + C::kTileBytes;
             const int key0 = kb + t * C::T;
             const int rows = min(C::T, ke - key0);  // rows this tile's copies wrote
-            // scores (log2 units): partial dot products over this lane's 8 dimensions,
-            // summed over the CH lanes of the key row
-            float sc[C::kSteps][NQ];
+            // no key of the tile is masked for any real row (the common case)
+            const bool full = rows == C::T && key0 + C::T <= lim_min;
+            if constexpr (NQ == 1) {
+                // scores (log2 units): partial dot products over this lane's 8 dimensions,
+                // summed over the CH lanes of the key row
+                float sc[C::kSteps];
 #pragma unroll
-            for (int st = 0; st < C::kSteps; ++st) {
-                const int key = st * C::G + grp;
-                float2 kf[4];
-                unpack8<BF16>(*reinterpret_cast<const uint4*>(sk + key * (D * 2) + ch * 16), kf);
-#pragma unroll
-                for (int r = 0; r < NQ; ++r) {
-                    float2 a = __fmul2_rn(qf[r][0], kf[0]);
-                    a = __ffma2_rn(qf[r][1], kf[1], a);
-                    a = __ffma2_rn(qf[r][2], kf[2], a);
-                    a = __ffma2_rn(qf[r][3], kf[3], a);
+                for (int st = 0; st < C::kSteps; ++st) {
+                    const int key = st * C::G + grp;
+                    float2 kf[4];
+                    unpack8<BF16>(*reinterpret_cast<const uint4*>(sk + key * (D * 2) + ch * 16), kf);
+                    float2 a = __fmul2_rn(qf[0][0], kf[0]);
+                    a = __ffma2_rn(qf[0][1], kf[1], a);
+                    a = __ffma2_rn(qf[0][2], kf[2], a);
+                    a = __ffma2_rn(qf[0][3], kf[3], a);
                     float x = a.x + a.y;
 #pragma unroll
                     for (int off = 1; off < C::CH; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-                    sc[st][r] = (key < rows && key0 + key < lim[r]) ? x : -INFINITY;
+                    sc[st] = (full || (key < rows && key0 + key < lim[0])) ? x : -INFINITY;
                 }
-            }
-            // online softmax over the tile, per row
-#pragma unroll
-            for (int r = 0; r < NQ; ++r) {
+                // online softmax over the tile
                 float mx = -INFINITY;
 #pragma unroll
-                for (int st = 0; st < C::kSteps; ++st) mx = fmaxf(mx, sc[st][r]);
+                for (int st = 0; st < C::kSteps; ++st) mx = fmaxf(mx, sc[st]);
 #pragma unroll
                 for (int off = C::CH; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float m_new = fmaxf(m[r], mx);
+                float m_new = fmaxf(m[0], mx);
+                if (m_new - m[0] <= kRescaleTau) m_new = m[0];  // keep the maximum (false from -inf)
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float alpha = ex2_ftz(m[r] - m_use);  // 0 from an empty state
-                m[r] = m_new;
-                l[r] *= alpha;
-                const float2 a2 = make_float2(alpha, alpha);
+                const float alpha = m[0] == m_use ? 1.f : ex2_ftz(m[0] - m_use);  // 0 from an empty state
+                m[0] = m_new;
+                if (alpha != 1.f) {  // warp-uniform: m is the warp's
+                    l[0] *= alpha;
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) o[r][e] = __fmul2_rn(o[r][e], a2);
+                    for (int e = 0; e < 4; ++e) o[0][e] = __fmul2_rn(o[0][e], a2);
+                }
 #pragma unroll
                 for (int st = 0; st < C::kSteps; ++st) {
-                    sc[st][r] = ex2_ftz(sc[st][r] - m_use);
-                    l[r] += sc[st][r];
+                    sc[st] = ex2_ftz(sc[st] - m_use);
+                    l[0] += sc[st];
                 }
-            }
-            // O += P V over this lane group's keys and this lane's 8 dimensions
+                // O += P V over this lane group's keys and this lane's 8 dimensions
 #pragma unroll
-            for (int st = 0; st < C::kSteps; ++st) {
-                const int key = st * C::G + grp;
-                if (key < rows) {
-                    float2 vf[4];
-                    unpack8<BF16>(*reinterpret_cast<const uint4*>(sv + key * (D * 2) + ch * 16), vf);
+                for (int st = 0; st < C::kSteps; ++st) {
+                    const int key = st * C::G + grp;
+                    if (full || key < rows) {
+                        float2 vf[4];
+                        unpack8<BF16>(*reinterpret_cast<const uint4*>(sv + key * (D * 2) + ch * 16), vf);
+                        const float2 p2 = make_float2(sc[st], sc[st]);
 #pragma unroll
-                    for (int r = 0; r < NQ; ++r) {
-                        const float2 p2 = make_float2(sc[st][r], sc[st][r]);
+                        for (int e = 0; e < 4; ++e) o[0][e] = __ffma2_rn(p2, vf[e], o[0][e]);
+                    }
+                }
+            } else {
+                // scores: four partial dot products per lane, then a transposed reduction
+                // over the CH lanes of the key row that leaves row rho's score in the lane
+                // (two partials exchanged across bit 2, one across bit 1, then plain sums)
+                float sc[C::kSteps];
+                const bool b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) o[r][e] = __ffma2_rn(p2, vf[e], o[r][e]);
+                for (int st = 0; st < C::kSteps; ++st) {
+                    const int key = st * C::G + grp;
+                    float2 kf[4];
+                    unpack8<BF16>(*reinterpret_cast<const uint4*>(sk + key * (D * 2) + ch * 16), kf);
+                    float x[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        float2 a = __fmul2_rn(qf[r][0], kf[0]);
+                        a = __ffma2_rn(qf[r][1], kf[1], a);
+                        a = __ffma2_rn(qf[r][2], kf[2], a);
+                        a = __ffma2_rn(qf[r][3], kf[3], a);
+                        x[r] = a.x + a.y;
+                    }
+                    // across bit 2: keep rows {0,1} (bit2 = 0) or {2,3}
+                    const float ka = b2 ? x[2] : x[0], kb2 = b2 ? x[3] : x[1];
+                    const float ga = b2 ? x[0] : x[2], gb = b2 ? x[1] : x[3];
+                    const float ya = ka + __shfl_xor_sync(0xffffffffu, ga, 4);
+                    const float yb = kb2 + __shfl_xor_sync(0xffffffffu, gb, 4);
+                    // across bit 1: keep row 2 * bit2 + bit1
+                    float z = (b1 ? yb : ya) + __shfl_xor_sync(0xffffffffu, b1 ? ya : yb, 2);
+                    z += __shfl_xor_sync(0xffffffffu, z, 1);
+                    if constexpr (C::CH == 16) z += __shfl_xor_sync(0xffffffffu, z, 8);
+                    sc[st] = (full || (key < rows && key0 + key < lim_rho)) ? z : -INFINITY;
+                }
+                // online softmax of row rho over the tile (state m[0], l[0] of that row)
+                float mx = -INFINITY;
+#pragma unroll
+                for (int st = 0; st < C::kSteps; ++st) mx = fmaxf(mx, sc[st]);
+#pragma unroll
+                for (int off = C::CH; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                float m_new = fmaxf(m[0], mx);
+                if (m_new - m[0] <= kRescaleTau) m_new = m[0];  // keep the maximum (false from -inf)
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = m[0] == m_use ? 1.f : ex2_ftz(m[0] - m_use);  // 0 from an empty state
+                m[0] = m_new;
+                l[0] *= alpha;
+#pragma unroll
+                for (int st = 0; st < C::kSteps; ++st) {
+                    sc[st] = ex2_ftz(sc[st] - m_use);
+                    l[0] += sc[st];
+                }
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {  // some row's maximum moved
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float ar = __shfl_sync(0xffffffffu, alpha, src(r));
+                        const float2 a2 = make_float2(ar, ar);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[r][e] = __fmul2_rn(o[r][e], a2);
+                    }
+                }
+                // O += P V: every row's P of the key fetched from its lane, then this lane's
+                // 8 dimensions of each row
+#pragma unroll
+                for (int st = 0; st < C::kSteps; ++st) {
+                    const int key = st * C::G + grp;
+                    float pr[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) pr[r] = __shfl_sync(0xffffffffu, sc[st], src(r));
+                    if (full || key < rows) {
+                        float2 vf[4];
+                        unpack8<BF16>(*reinterpret_cast<const uint4*>(sv + key * (D * 2) + ch * 16), vf);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float2 p2 = make_float2(pr[r], pr[r]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) o[r][e] = __ffma2_rn(p2, vf[e], o[r][e]);
+                        }
                     }
                 }
             }
@@ -238,16 +333,25 @@ __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1) attn_decode_kernel
         if (!ok) break;
         // sum the lane groups' l and O (all relative to the same m)
 #pragma unroll
+        for (int off = C::CH; off < 32; off <<= 1) l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+#pragma unroll
         for (int r = 0; r < NQ; ++r)
 #pragma unroll
             for (int off = C::CH; off < 32; off <<= 1) {
-                l[r] += __shfl_xor_sync(0xffffffffu, l[r], off);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     o[r][e].x += __shfl_xor_sync(0xffffffffu, o[r][e].x, off);
                     o[r][e].y += __shfl_xor_sync(0xffffffffu, o[r][e].y, off);
                 }
             }
+        if constexpr (NQ > 1) {  // row r's l and m from the lanes that hold row r
+            const float l_own = l[0], m_own = m[0];
+#pragma unroll
+            for (int r = 0; r < NQ; ++r) {
+                l[r] = __shfl_sync(0xffffffffu, l_own, src(r));
+                m[r] = __shfl_sync(0xffffffffu, m_own, src(r));
+            }
+        }
         const int rg = u - bh * p.n_ranges;
 #pragma unroll
         for (int r = 0; r < NQ; ++r) {

@@ -88,10 +88,11 @@ struct DecodePlan {
 };
 // Keys per K/V tile and warps per CTA of the decode kernel (one CTA per SM, 192 KB of
 // shared memory at most) for head dimension d and Nq query rows: 32-key tiles (copies of
-// 8 or 16 KB) where the registers allow a warp per SMSP or more, 16-key tiles to fit
-// three warps per SMSP for several rows at d = 64.
-constexpr int decode_tile_keys(int64_t d, int64_t nq) { return d == 64 && nq > 1 ? 16 : 32; }
+// 8 or 16 KB); as many warps as the registers allow, three stages per warp (two for
+// several rows at d = 64, whose twelve warps would not fit three).
+constexpr int decode_tile_keys(int64_t, int64_t) { return 32; }
 constexpr int decode_warps(int64_t d, int64_t nq) { return d == 128 ? 4 : (nq == 1 ? 8 : 12); }
+constexpr int decode_stages(int64_t d, int64_t nq) { return d == 64 && nq > 1 ? 2 : 3; }
 DecodePlan plan_decode(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, size_t ws_bytes, int64_t sms);
 cudaError_t launch_decode(int64_t d, bool bf16, const DecodeParams& p, int64_t grid, cudaStream_t s);
 

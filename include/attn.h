@@ -129,7 +129,7 @@ int attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float
  *    sees no key (bottom-right with Nq > Nk) gets O = 0 and LSE = -inf.
  *  - Nq <= 4: a streaming kernel on the CUDA cores runs instead of the tensor-core
  *    kernel (a decode step reads each K and V byte for at most four rows, so the
- *    call is bound by HBM). Each warp streams K and V tiles of 16 keys with bulk
+ *    call is bound by HBM). Each warp streams K and V tiles of 32 keys with bulk
  *    copies and keeps P and every sum in fp32. Its keys are cut into ranges as a
  *    balance model of the grid's warps favours; with a workspace, the ranges'
  *    fp32 partial outputs go there and a second kernel merges them, and with

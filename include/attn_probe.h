@@ -67,7 +67,7 @@ int64_t attn_probe_plan_host(int64_t BH, int64_t N, int64_t sms, int64_t* heads_
  * attn_probe_plan_decode -- the plan of the streaming decode kernel that attn_fwd_kv
  * runs for Nq <= 4 without padding or window, for a GPU with `sms` SMs and a
  * workspace of `ws_bytes`: out[0] = key ranges per head (1: no workspace used, the
- * kernel writes O and LSE itself), out[1] = keys per range (a multiple of 16),
+ * kernel writes O and LSE itself), out[1] = keys per range (a multiple of 32),
  * out[2] = CTAs launched, out[3] = workspace bytes the plan uses. Host arithmetic
  * only. Returns ATTN_ERR_INVALID_ARG for sizes outside the decode kernel's range.
  */

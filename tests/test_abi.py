@@ -363,20 +363,20 @@ def test_planners_follow_the_sm_count(lib):
 
 
 def test_decode_planner(lib):
-    """The streaming decode kernel's plan: key ranges of whole tiles (32 keys; 16 for
-    several rows at d = 64) covering every key, the workspace the partials need (none for one range), at most one CTA per SM,
+    """The streaming decode kernel's plan: key ranges of whole 32-key tiles covering every
+    key, the workspace the partials need (none for one range), at most one CTA per SM,
     capped by the workspace, and the plans of the three decode workloads on 152 SMs."""
     from exact_attention_61_gb300 import attn
     full = 1 << 40
     # (BH, Nq, Nk, d) -> (ranges, keys per range)
     assert attn.plan_decode_for(256, 1, 8192, 128, full, 152)[:2] == (7, 1184)
     assert attn.plan_decode_for(16, 1, 65536, 128, full, 152)[:2] == (38, 1728)
-    assert attn.plan_decode_for(256, 4, 4096, 64, full, 152)[:2] == (7, 592)
+    assert attn.plan_decode_for(256, 4, 4096, 64, full, 152)[:2] == (7, 608)
     for sms in (1, 16, 132, 148, 152, 200):
         for BH, Nq, Nk, d in ((1, 1, 1, 64), (1, 1, 65536, 128), (256, 4, 4096, 64), (300, 3, 1 << 20, 64),
                               (5, 2, 777, 128), (4096, 1, 100, 128)):
             n, rk, grid, nbytes = attn.plan_decode_for(BH, Nq, Nk, d, full, sms)
-            assert rk % (16 if d == 64 and Nq > 1 else 32) == 0 and rk * (n - 1) < Nk <= rk * n
+            assert rk % 32 == 0 and rk * (n - 1) < Nk <= rk * n
             assert nbytes == (0 if n == 1 else BH * n * Nq * (d + 1) * 4)
             warps = 4 if d == 128 else (8 if Nq == 1 else 12)
             assert 1 <= grid <= sms and grid == min(sms, -(-BH * n // warps))
