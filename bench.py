@@ -594,8 +594,9 @@ def decode_bytes(B_: int, H_: int, Nq: int, Nk: int, d: int, elem: int = 2) -> i
 
 def run_decode(args) -> int:
     """--decode NAME: one KV-cache decode step per timed step (attn_fwd_kv, bottom-right
-    causal mask, split of the keys + merge), reported as HBM GB/s against the measured
-    copy bandwidth. Single GPU; an extra measurement beside the headline line."""
+    causal mask: the streaming decode kernel over key ranges, then the merge), reported as
+    HBM GB/s against the measured copy bandwidth. Single GPU; an extra measurement beside
+    the headline line."""
     import torch
 
     from exact_attention_61_gb300 import attn
@@ -651,7 +652,8 @@ def run_decode(args) -> int:
     nbytes = decode_bytes(w.B, w.H, w.Nq, w.Nk, w.d)
     gbs = nbytes / (ms * 1e-3) / 1e9
     peaks = measured_peaks()
-    splits = ws_n // (w.B * w.H * w.Nq * (w.d + 1) * 4) if ws_n else 1
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    splits = attn.plan_decode_for(w.B * w.H, w.Nq, w.Nk, w.d, ws_n, sms)[0]  # key ranges per head
     out = {
         "metric": f"decode attention HBM GB/s ({w.name})", "value": gbs, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": n_warm, "ms_per_step": ms, "higher_is_better": True,
@@ -660,7 +662,7 @@ def run_decode(args) -> int:
                    "mask": "causal_bottom_right", "key_splits": splits, "seed": w.seed,
                    "l2": "flushed before every step (write of 2x L2 size, outside the events)"},
         "ms_median": statistics.median(t_ms), "ms_p10": _pct(t_ms, 10), "ms_p90": _pct(t_ms, 90),
-        "roofline": {"bound": "hbm", "kernel": "attn_fwd_kernel split + attn_merge_kernel (one call)",
+        "roofline": {"bound": "hbm", "kernel": "attn_decode_kernel + attn_merge_kernel (one call)",
                      "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": None,
                      "algorithmic_bytes_per_step": nbytes,
