@@ -39,6 +39,7 @@
 namespace attn_sm103 {
 
 enum : uint32_t { kRoleBwdLoad = 5, kRoleBwdMma = 6, kRoleBwdCompute = 7, kRoleBwdDq = 8 };
+constexpr int kBwdHeadGroup = 8;  // heads whose causal key tiles are ordered together
 constexpr uint32_t kErrSmemAlign = 2u;
 
 // ---- tcgen05 / bulk-copy forms only the backward uses ------------------------------------
@@ -154,7 +155,12 @@ struct BwdCfg {
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kTileBytes;
     static constexpr int kOffDS = kOffV + kTileBytes;   // dS: 128 keys x 128 queries, MN-major
-    static constexpr int kOffStage = kOffDS + 128 * 128 * 2;
+    // d = 64: S^T and dP^T of the next Q tile are issued before dQ of the current one, so
+    // its compute overlaps that product; dS then alternates between two buffers (d = 128
+    // keeps its dQ tile over S^T and the plain order).
+    static constexpr bool kEarlyNext = D == 64;
+    static constexpr int kDsBufs = kEarlyNext ? 2 : 1;
+    static constexpr int kOffStage = kOffDS + kDsBufs * 128 * 128 * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;  // Q, then dO
     // The fp32 dQ tile (128 rows x d, exactly one Q/dO ring stage) is staged in the ring
     // stage of its own iteration, in boxes of 32 columns x 128 rows with the 128-byte
@@ -216,9 +222,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     auto sDO = [&](int s) -> uint32_t { return sQ(s) + C::kTileBytes; };
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem_bwd + C::kOffMisc);  // [0] tmem, [1] abort
 
-    // Heaviest key tiles first: under the causal mask key tile 0 sees every Q tile.
-    const int bh = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.BH));
-    const int kt = static_cast<int>(blockIdx.x / static_cast<uint32_t>(p.BH));
+    // CTA order. Non-causal: a head's key tiles run together, so its Q, dO and dQ
+    // accumulator stay in L2. Causal: heads in groups of kBwdHeadGroup, whose key tiles run
+    // heaviest first (key tile 0 sees every Q tile), so the group's working set stays in L2
+    // and the grid still ends on light tiles.
+    const int n_kt_grid = static_cast<int>(gridDim.x) / p.BH;
+    int bh, kt;
+    if (CAUSAL) {
+        const int x = static_cast<int>(blockIdx.x);
+        const int grp = x / (kBwdHeadGroup * n_kt_grid);
+        const int gh = min(kBwdHeadGroup, p.BH - grp * kBwdHeadGroup);  // heads in this group
+        const int idx = x - grp * kBwdHeadGroup * n_kt_grid;
+        kt = idx / gh;
+        bh = grp * kBwdHeadGroup + idx % gh;
+    } else {
+        bh = static_cast<int>(blockIdx.x) / n_kt_grid;
+        kt = static_cast<int>(blockIdx.x) % n_kt_grid;
+    }
     const int Nq = p.Nq, Nk = p.Nk;
     const int j0 = kt * 128;
     // Valid keys of this batch element; key j is visible to query row i iff j < n_b and,
@@ -320,25 +340,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint64_t dQ_k0 = sdesc_sw128(sQ(0), 16, 1024);
         const uint64_t dQ_mn0 = sdesc_sw128(sQ(0), C::kBoxBytes, 1024);
 
-        bool ok = wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdMma * 1000 + C::kBarKV, 0);
-        for (int it = 0; it < n_it && ok; ++it) {
-            const int s = it % C::kStages;
-            if (!wait_warp(bar(C::kBarQdFull + s), (it / C::kStages) & 1, wc,
-                           kRoleBwdMma * 1000 + C::kBarQdFull + s, it)) {
-                ok = false;
-                break;
-            }
-            // d = 128: the dQ tile of the previous iteration lives in the S^T columns.
-            if (D == 128 && it > 0 &&
-                !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
-                ok = false;
-                break;
-            }
+        // S^T = K Q^T and dP^T = V dO^T of iteration i (its Q/dO stage full), then a commit.
+        auto issue_sdp = [&](int i) -> bool {
+            const int si = i % C::kStages;
+            if (!wait_warp(bar(C::kBarQdFull + si), (i / C::kStages) & 1, wc, kRoleBwdMma * 1000 + C::kBarQdFull + si,
+                           i))
+                return false;
             tc_fence_after_sync();
-            const uint64_t q_k = dQ_k0 + s * kStageStep;
+            const uint64_t q_k = dQ_k0 + si * kStageStep;
             const uint64_t do_k = q_k + kTileStep;
-            const uint64_t q_mn = dQ_mn0 + s * kStageStep;
-            const uint64_t do_mn = q_mn + kTileStep;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
                 const uint64_t off = (c * C::kBoxBytes) >> 4;
@@ -350,13 +360,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 mma_qk64_warp(tmem + C::colDP, dV_k + off, do_k + off, idesc_s, c > 0 ? 1u : 0u);
             }
             mma_commit_warp(bar(C::kBarSdp));
+            return true;
+        };
+
+        bool ok = wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdMma * 1000 + C::kBarKV, 0);
+        if (C::kEarlyNext && ok && n_it > 0) ok = issue_sdp(0);
+        for (int it = 0; it < n_it && ok; ++it) {
+            const int s = it % C::kStages;
+            if (!C::kEarlyNext) {
+                // d = 128: the dQ tile of the previous iteration lives in the S^T columns.
+                if (it > 0 &&
+                    !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
+                    ok = false;
+                    break;
+                }
+                if (!issue_sdp(it)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (!wait_warp(bar(C::kBarPds), it & 1, wc, kRoleBwdMma * 1000 + C::kBarPds, it)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
+            const uint64_t q_mn = dQ_mn0 + s * kStageStep;
+            const uint64_t do_mn = q_mn + kTileStep;
             mma_pv128_halves_warp(tmem + C::colDV, tmem + C::colS, do_mn, idesc_o, it > 0 ? 1u : 0u);
             mma_pv128_halves_warp(tmem + C::colDK, tmem + C::colDP, q_mn, idesc_o, it > 0 ? 1u : 0u);
+            // d = 64: S^T/dP^T of the next iteration overwrite P^T/dS^T only after dV and dK
+            // (issue order); its compute overlaps the dQ product below, which reads the
+            // other dS buffer.
+            if (C::kEarlyNext && it + 1 < n_it && !issue_sdp(it + 1)) {
+                ok = false;
+                break;
+            }
             // d = 64: the dQ columns of the previous iteration must have been read out.
             if (D == 64 && it > 0 &&
                 !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
@@ -364,7 +402,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            mma_mn128_warp(tmem + C::colDQ, dDS, dK_mn, idesc_q, 0u);
+            mma_mn128_warp(tmem + C::colDQ, dDS + (C::kEarlyNext ? ((it & 1) * (128 * 128 * 2)) >> 4 : 0), dK_mn,
+                           idesc_q, 0u);
             mma_commit_warp(bar(C::kBarDqFull));
             mma_commit_warp(bar(C::kBarQdEmpty + s));
         }
@@ -429,7 +468,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
         const float qk = p.qk_scale;
         const float2 qk2 = make_float2(qk, qk);
-        const uint32_t sDS = base + C::kOffDS + h * C::kBoxBytes + r * 128u;
+        const uint32_t sDS0 = base + C::kOffDS + h * C::kBoxBytes + r * 128u;
         bool ok = true;
         for (int it = 0; it < n_it && ok; ++it) {
             const int s = it % C::kStages;
@@ -440,9 +479,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 ok = false;
                 break;
             }
-            // S^T(it) and dP^T(it) complete also means the dQ product of the previous
-            // iteration (issued before them) has finished reading the dS tile.
+            // S^T(it) and dP^T(it) complete also means the dQ product that last read this
+            // iteration's dS buffer (iteration it-1, or it-2 with two buffers; issued before
+            // them) has finished reading it.
             tc_fence_after_sync();
+            const uint32_t sDS = sDS0 + (C::kEarlyNext ? (it & 1) * (128 * 128 * 2) : 0);
             const float* vec = reinterpret_cast<const float*>(smem_bwd + C::kOffVec + s * C::kVecBytes);
             const float* nlse2 = vec + 64 * h;        // -LSE log2(e) of this half's query rows
             const float* ndvec = vec + 128 + 64 * h;  // -D
