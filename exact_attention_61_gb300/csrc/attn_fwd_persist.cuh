@@ -414,6 +414,8 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                     if (m_new - m <= kRescaleTau) m_new = m;
                     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                     alpha = (m == m_use) ? 1.f : ex2_ftz(m - m_use);
+                    // whether any row of the warp rescales O: decided here, off the P hand-off
+                    rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
                     const float2 neg_m2 = make_float2(-m_use, -m_use);
                     uint32_t pk[2][32];
                     float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -436,7 +438,6 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 1)
                 }
                 // Rescale O_t once O_t += P V of this tile's previous job has completed
                 // (every earlier one has: see the parity argument at the o_done waits).
-                rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
                 if (rescale && ok)
                     ok = wait_warp(bar(C::kBarODone + t * 2 + ((kk - 1) & 1)), ((kk - 1) >> 1) & 1, wc,
                                    role * 1000 + C::kBarODone + t * 2, j);
