@@ -95,11 +95,10 @@ __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1) attn_decode_kernel
         if (p.causal) e = p.align_br ? r + p.Nk - p.Nq + 1 : r + 1;
         lim[r] = r < p.Nq ? max(0, min(p.Nk, e)) : 0;
     }
-    int vis = 0;       // keys any row sees
-    int lim_min = vis;  // keys every real row sees
+    int vis = 0;  // keys any row sees
 #pragma unroll
     for (int r = 0; r < NQ; ++r) vis = max(vis, lim[r]);
-    lim_min = vis;
+    int lim_min = vis;  // keys every real row sees
 #pragma unroll
     for (int r = 0; r < NQ; ++r)
         if (r < p.Nq) lim_min = min(lim_min, lim[r]);
