@@ -18,14 +18,16 @@
 //    mask). K and V stay in shared memory; Q, dO and the per-row LSE/D vectors
 //    stream through a TMA ring;
 //  - one warp issues the tcgen05 MMAs, all into tensor memory:
-//      S^T  = K Q^T     (128 keys x 128 queries, fp32)
-//      dP^T = V dO^T    (128 x 128, fp32)
+//      S^T  = K Q^T     (128 keys x 128 queries, fp32; d = 64: K from TMEM)
+//      dP^T = V dO^T    (128 x 128, fp32; d = 64: V from TMEM)
 //      dV  += P^T dO    (P^T 16-bit in TMEM over S^T; dO MN-major in SMEM)
 //      dK  += dS^T Q    (dS^T 16-bit in TMEM over dP^T; Q MN-major in SMEM)
 //      dQ   = dS K      (dS 16-bit in SMEM, MN-major; K MN-major in SMEM)
 //  - two warpgroups, one thread per key row (= TMEM lane) and half of the 128
 //    query columns each, turn S^T and dP^T into P^T and dS^T with exp2 and the
-//    LSE folded in log2 units, and write dS for the dQ product to shared memory;
+//    LSE folded in log2 units, and write dS for the dQ product to shared memory.
+//    At d = 64 each half has its own S^T/dP^T and P^T/dS^T hand-off, so one
+//    warpgroup's math overlaps the other half's products;
 //  - a third warpgroup adds each dQ tile into an fp32 workspace (dQ gathers over key
 //    tiles owned by other CTAs) by staging it in shared memory and a TMA bulk
 //    reduce-add, off the critical path of the other two;
@@ -102,6 +104,52 @@ __device__ __forceinline__ void mma_pv128_halves_warp(uint32_t d_tmem, uint32_t 
         : "memory");
 }
 
+// D (+)= A B over 64 rows of K with A (16-bit) in TMEM columns [a, a+32) and B MN-major
+// in SMEM: 4 MMAs of K = 16, A advancing 8 columns and B 16 rows = 128 descriptor units.
+// `accumulate` applies to the first MMA.
+__device__ __forceinline__ void mma_pv64_tmem_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, one;\n\t.reg .b32 ta;\n\t.reg .b64 bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 one, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.u64 bd, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.u64 bd, %2, 256;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.u64 bd, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D = A B^T over K = 64 with A (16-bit, M x 64) in TMEM columns [a, a+32) and B K-major
+// in SMEM (128-byte swizzle): 4 MMAs of K = 16, A advancing 8 columns and B 32 bytes.
+__device__ __forceinline__ void mma_ts_k64_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred e, zero, one;\n\t.reg .b32 ta;\n\t.reg .b64 bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 zero, 0, 0;\n\t"
+        "setp.eq.b32 one, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, zero;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.u64 bd, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.u64 bd, %2, 4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.u64 bd, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, one;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr)
+                 : "memory");
+}
+
 // Instruction descriptor with the major-ness of A chosen too (bit 15; A from SMEM).
 __host__ __device__ constexpr uint32_t idesc_f16_f32acc_ab(bool bf16, int M, int N, bool a_mn_major,
                                                            bool b_mn_major) {
@@ -155,9 +203,11 @@ struct BwdCfg {
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kTileBytes;
     static constexpr int kOffDS = kOffV + kTileBytes;   // dS: 128 keys x 128 queries, MN-major
-    // d = 64: S^T and dP^T of the next Q tile are issued before dQ of the current one, so
-    // its compute overlaps that product; dS then alternates between two buffers (d = 128
-    // keeps its dQ tile over S^T and the plain order).
+    // d = 64: a Q tile is two halves of 64 query columns, one per compute warpgroup, each
+    // with its own S^T/dP^T commit and P^T/dS^T hand-off. S^T and dP^T of half h of the next
+    // tile are issued right after dV and dK of half h of this one, before dQ, so one
+    // warpgroup's math overlaps the other half's products and dQ; dS then alternates
+    // between two buffers (d = 128 keeps its dQ tile over S^T and the plain order).
     static constexpr bool kEarlyNext = D == 64;
     static constexpr int kDsBufs = kEarlyNext ? 2 : 1;
     static constexpr int kOffStage = kOffDS + kDsBufs * 128 * 128 * 2;
@@ -175,12 +225,13 @@ struct BwdCfg {
     static constexpr int kBarKV = 0;
     static constexpr int kBarQdFull = 1;
     static constexpr int kBarQdEmpty = kBarQdFull + kStages;
-    static constexpr int kBarSdp = kBarQdEmpty + kStages;  // S^T and dP^T in TMEM
-    static constexpr int kBarPds = kBarSdp + 1;            // P^T, dS^T in TMEM and dS in SMEM
-    static constexpr int kBarDqFull = kBarPds + 1;         // dQ tile in TMEM
+    static constexpr int kBarSdp = kBarQdEmpty + kStages;  // [half]: S^T and dP^T in TMEM
+    static constexpr int kBarPds = kBarSdp + 2;            // [half]: P^T, dS^T in TMEM, dS in SMEM
+    static constexpr int kBarDqFull = kBarPds + 2;         // dQ tile in TMEM
     static constexpr int kBarDqRead = kBarDqFull + 1;      // dQ tile read out
     static constexpr int kBarAcc = kBarDqRead + 1;         // dK, dV final
-    static constexpr int kBarDrain = kBarAcc + 1;
+    static constexpr int kBarKvTmem = kBarAcc + 1;         // d = 64: K and V copied into TMEM
+    static constexpr int kBarDrain = kBarKvTmem + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     // The dynamic shared-memory base is 1024-byte aligned (declared so and checked at
@@ -190,7 +241,12 @@ struct BwdCfg {
     // TMEM columns: S^T/P^T, dP^T/dS^T, dV, dK, and the dQ tile (d = 128: over S^T).
     static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
     static constexpr uint32_t colDQ = D == 64 ? 384u : 0u;
+    // d = 64: K and V (16-bit, two elements per column) are the A operands of S^T and dP^T
+    // from TMEM, so the tensor core reads only Q and dO from shared memory for them.
+    static constexpr bool kKvTmem = kEarlyNext;
+    static constexpr uint32_t colK = 448, colV = 480;
     static constexpr uint32_t kTmemCols = 512;
+    static_assert(!kKvTmem || (colDQ + D <= colK && colV + D / 2 <= kTmemCols), "TMEM budget");
     // warps 0-3: compute, query columns 0-63; 4-7: compute, columns 64-127;
     // 8-11: dQ read-out; 12: MMA; 13: TMA
     static constexpr int kThreads = 448;
@@ -269,8 +325,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             uint32_t count = 1;
             if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages)
                 count = 1 + 8 + 1;  // MMA, compute warps, dQ store
-            if (i == C::kBarPds) count = 8;                                              // compute warps
-            if (i == C::kBarDqRead) count = 4;                                           // dQ warps
+            if (i == C::kBarPds || i == C::kBarPds + 1) count = C::kEarlyNext ? 4 : 8;  // compute warps
+            if (i == C::kBarDqRead || i == C::kBarKvTmem) count = 4;                     // dQ warps
             mbar_init(bar(i), count);
         }
         misc[1] = 0u;
@@ -340,72 +396,95 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint64_t dQ_k0 = sdesc_sw128(sQ(0), 16, 1024);
         const uint64_t dQ_mn0 = sdesc_sw128(sQ(0), C::kBoxBytes, 1024);
 
-        // S^T = K Q^T and dP^T = V dO^T of iteration i (its Q/dO stage full), then a commit.
-        auto issue_sdp = [&](int i) -> bool {
-            const int si = i % C::kStages;
-            if (!wait_warp(bar(C::kBarQdFull + si), (i / C::kStages) & 1, wc, kRoleBwdMma * 1000 + C::kBarQdFull + si,
-                           i))
-                return false;
-            tc_fence_after_sync();
-            const uint64_t q_k = dQ_k0 + si * kStageStep;
-            const uint64_t do_k = q_k + kTileStep;
-#pragma unroll
-            for (int c = 0; c < C::kChunks; ++c) {
-                const uint64_t off = (c * C::kBoxBytes) >> 4;
-                mma_qk64_warp(tmem + C::colS, dK_k + off, q_k + off, idesc_s, c > 0 ? 1u : 0u);
+        // d = 64: the dQ warps copy K and V into TMEM once they have landed (which also
+        // means K is in shared memory for dQ).
+        bool ok = C::kKvTmem ? wait_warp(bar(C::kBarKvTmem), 0, wc, kRoleBwdMma * 1000 + C::kBarKvTmem, 0)
+                             : wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdMma * 1000 + C::kBarKV, 0);
+        if (ok) tc_fence_after_sync();
+        if constexpr (C::kEarlyNext) {
+            // d = 64, per Q tile: for each half h (query columns [64h, 64h + 64), warpgroup
+            // h), once its P^T/dS^T are ready: dV += P_h^T dO_h and dK += dS_h^T Q_h (K = 64
+            // queries), then S^T/dP^T of half h of the next tile, which overwrite P_h^T/dS_h^T
+            // only after dV and dK have read them (issue order). dQ of the tile comes last.
+            constexpr uint32_t idesc_h = idesc_f16_f32acc(BF16, 128, 64, false);  // N = 64 queries
+            constexpr uint64_t kHalfRows = (64 * 128) >> 4;  // 64 rows of a 128-byte-swizzled box
+            auto issue_sdp_half = [&](int i, int h) -> bool {
+                const int si = i % C::kStages;
+                if (h == 0 && !wait_warp_sleep(bar(C::kBarQdFull + si), (i / C::kStages) & 1, wc,
+                                         kRoleBwdMma * 1000 + C::kBarQdFull + si, i))
+                    return false;
+                tc_fence_after_sync();
+                const uint64_t q_k = dQ_k0 + si * kStageStep + h * kHalfRows;
+                mma_ts_k64_warp(tmem + C::colS + 64u * h, tmem + C::colK, q_k, idesc_h);
+                mma_ts_k64_warp(tmem + C::colDP + 64u * h, tmem + C::colV, q_k + kTileStep, idesc_h);
+                mma_commit_warp(bar(C::kBarSdp + h));
+                return true;
+            };
+            if (ok && n_it > 0) ok = issue_sdp_half(0, 0) && issue_sdp_half(0, 1);
+            for (int it = 0; it < n_it && ok; ++it) {
+                const int s = it % C::kStages;
+                const uint64_t q_mn = dQ_mn0 + s * kStageStep;
+                const uint64_t do_mn = q_mn + kTileStep;
+                for (int h = 0; h < 2 && ok; ++h) {
+                    ok = wait_warp_sleep(bar(C::kBarPds + h), it & 1, wc, kRoleBwdMma * 1000 + C::kBarPds + h, it);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t acc = (it > 0 || h > 0) ? 1u : 0u;
+                    mma_pv64_tmem_warp(tmem + C::colDV, tmem + C::colS + 64u * h, do_mn + h * kHalfRows, idesc_o, acc);
+                    mma_pv64_tmem_warp(tmem + C::colDK, tmem + C::colDP + 64u * h, q_mn + h * kHalfRows, idesc_o, acc);
+                    if (it + 1 < n_it) ok = issue_sdp_half(it + 1, h);
+                }
+                // The dQ columns of the previous tile must have been read out.
+                if (ok && it > 0)
+                    ok = wait_warp_sleep(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it);
+                if (!ok) break;
+                tc_fence_after_sync();
+                mma_mn128_warp(tmem + C::colDQ, dDS + (((it & 1) * (128 * 128 * 2)) >> 4), dK_mn, idesc_q, 0u);
+                mma_commit_warp(bar(C::kBarDqFull));
+                mma_commit_warp(bar(C::kBarQdEmpty + s));
             }
-#pragma unroll
-            for (int c = 0; c < C::kChunks; ++c) {
-                const uint64_t off = (c * C::kBoxBytes) >> 4;
-                mma_qk64_warp(tmem + C::colDP, dV_k + off, do_k + off, idesc_s, c > 0 ? 1u : 0u);
-            }
-            mma_commit_warp(bar(C::kBarSdp));
-            return true;
-        };
-
-        bool ok = wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdMma * 1000 + C::kBarKV, 0);
-        if (C::kEarlyNext && ok && n_it > 0) ok = issue_sdp(0);
-        for (int it = 0; it < n_it && ok; ++it) {
-            const int s = it % C::kStages;
-            if (!C::kEarlyNext) {
-                // d = 128: the dQ tile of the previous iteration lives in the S^T columns.
+        } else {
+            // d = 128, per Q tile: S^T and dP^T (the dQ tile of the previous one lives in the
+            // S^T columns, so it must have been read out), then dV, dK and dQ.
+            for (int it = 0; it < n_it && ok; ++it) {
+                const int s = it % C::kStages;
                 if (it > 0 &&
                     !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
                     ok = false;
                     break;
                 }
-                if (!issue_sdp(it)) {
+                if (!wait_warp(bar(C::kBarQdFull + s), (it / C::kStages) & 1, wc,
+                               kRoleBwdMma * 1000 + C::kBarQdFull + s, it)) {
                     ok = false;
                     break;
                 }
+                tc_fence_after_sync();
+                const uint64_t q_k = dQ_k0 + s * kStageStep;
+                const uint64_t do_k = q_k + kTileStep;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    const uint64_t off = (c * C::kBoxBytes) >> 4;
+                    mma_qk64_warp(tmem + C::colS, dK_k + off, q_k + off, idesc_s, c > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    const uint64_t off = (c * C::kBoxBytes) >> 4;
+                    mma_qk64_warp(tmem + C::colDP, dV_k + off, do_k + off, idesc_s, c > 0 ? 1u : 0u);
+                }
+                mma_commit_warp(bar(C::kBarSdp));
+                if (!wait_warp(bar(C::kBarPds), it & 1, wc, kRoleBwdMma * 1000 + C::kBarPds, it)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint64_t q_mn = dQ_mn0 + s * kStageStep;
+                const uint64_t do_mn = q_mn + kTileStep;
+                mma_pv128_halves_warp(tmem + C::colDV, tmem + C::colS, do_mn, idesc_o, it > 0 ? 1u : 0u);
+                mma_pv128_halves_warp(tmem + C::colDK, tmem + C::colDP, q_mn, idesc_o, it > 0 ? 1u : 0u);
+                mma_mn128_warp(tmem + C::colDQ, dDS, dK_mn, idesc_q, 0u);
+                mma_commit_warp(bar(C::kBarDqFull));
+                mma_commit_warp(bar(C::kBarQdEmpty + s));
             }
-            if (!wait_warp(bar(C::kBarPds), it & 1, wc, kRoleBwdMma * 1000 + C::kBarPds, it)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            const uint64_t q_mn = dQ_mn0 + s * kStageStep;
-            const uint64_t do_mn = q_mn + kTileStep;
-            mma_pv128_halves_warp(tmem + C::colDV, tmem + C::colS, do_mn, idesc_o, it > 0 ? 1u : 0u);
-            mma_pv128_halves_warp(tmem + C::colDK, tmem + C::colDP, q_mn, idesc_o, it > 0 ? 1u : 0u);
-            // d = 64: S^T/dP^T of the next iteration overwrite P^T/dS^T only after dV and dK
-            // (issue order); its compute overlaps the dQ product below, which reads the
-            // other dS buffer.
-            if (C::kEarlyNext && it + 1 < n_it && !issue_sdp(it + 1)) {
-                ok = false;
-                break;
-            }
-            // d = 64: the dQ columns of the previous iteration must have been read out.
-            if (D == 64 && it > 0 &&
-                !wait_warp(bar(C::kBarDqRead), (it - 1) & 1, wc, kRoleBwdMma * 1000 + C::kBarDqRead, it)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            mma_mn128_warp(tmem + C::colDQ, dDS + (C::kEarlyNext ? ((it & 1) * (128 * 128 * 2)) >> 4 : 0), dK_mn,
-                           idesc_q, 0u);
-            mma_commit_warp(bar(C::kBarDqFull));
-            mma_commit_warp(bar(C::kBarQdEmpty + s));
         }
         if (ok) mma_commit_warp(bar(C::kBarAcc));
         // Drain: all MMAs issued by this warp are complete before TMEM is freed.
@@ -422,8 +501,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
         const bool leader = warp == C::kWarpDq && lane == 0;
         if (leader) tma_prefetch_desc(&tmDQ);
+        if constexpr (C::kKvTmem) {
+            // K and V rows (128-byte-swizzled in shared memory) into TMEM lane r, 16-bit
+            // pairs per column: the A operands of S^T and dP^T.
+            const bool kv_ok = wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdDq * 1000 + C::kBarKV, 0);
+            if (kv_ok) {
+#pragma unroll 1
+                for (int m = 0; m < 2; ++m) {
+                    const uint32_t row = base + (m ? C::kOffV : C::kOffK) + r * 128u;
+                    uint32_t x[32];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        ld_shared_v4(row + ((ch ^ (r & 7u)) << 4), x[4 * ch], x[4 * ch + 1], x[4 * ch + 2], x[4 * ch + 3]);
+                    tmem_st32(lane_base + (m ? C::colV : C::colK), x);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0 && kv_ok) mbar_arrive(bar(C::kBarKvTmem));
+        }
         for (int it = 0; it < n_it; ++it) {
-            if (!wait_warp(bar(C::kBarDqFull), it & 1, wc, kRoleBwdDq * 1000 + C::kBarDqFull, it)) break;
+            if (!wait_warp_sleep(bar(C::kBarDqFull), it & 1, wc, kRoleBwdDq * 1000 + C::kBarDqFull, it)) break;
             tc_fence_after_sync();
             const int q0 = (qt0 + it) * 128;
             const int s = it % C::kStages;
@@ -469,13 +568,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const float qk = p.qk_scale;
         const float2 qk2 = make_float2(qk, qk);
         const uint32_t sDS0 = base + C::kOffDS + h * C::kBoxBytes + r * 128u;
+        const int hb = C::kEarlyNext ? static_cast<int>(h) : 0;  // this half's S/dP and P/dS barriers
         bool ok = true;
         for (int it = 0; it < n_it && ok; ++it) {
             const int s = it % C::kStages;
             const int q0 = (qt0 + it) * 128;
-            if (!wait_warp(bar(C::kBarQdFull + s), (it / C::kStages) & 1, wc,
+            if (!wait_warp_sleep(bar(C::kBarQdFull + s), (it / C::kStages) & 1, wc,
                            kRoleBwdCompute * 1000 + C::kBarQdFull + s, it) ||
-                !wait_warp(bar(C::kBarSdp), it & 1, wc, kRoleBwdCompute * 1000 + C::kBarSdp, it)) {
+                !wait_warp_sleep(bar(C::kBarSdp + hb), it & 1, wc, kRoleBwdCompute * 1000 + C::kBarSdp + hb, it)) {
                 ok = false;
                 break;
             }
@@ -547,7 +647,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(bar(C::kBarPds));
+                mbar_arrive(bar(C::kBarPds + hb));
                 mbar_arrive(bar(C::kBarQdEmpty + s));
             }
         }
