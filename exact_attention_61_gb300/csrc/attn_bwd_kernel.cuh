@@ -196,13 +196,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 template <int D>
 struct BwdCfg {
     static_assert(D == 64 || D == 128, "head dimension must be 64 or 128");
-    static constexpr int kStages = D == 64 ? 3 : 2;    // Q/dO ring depth
+    // Q/dO ring depth. Each stage is held until the dQ reduce-add of its tile has read
+    // it, so the ring also absorbs the latency of those L2 reductions.
+    static constexpr int kStages = D == 64 ? 4 : 2;
     static constexpr int kBoxBytes = 128 * 128;         // one TMA box: 128 rows x 64 elements x 2 B
     static constexpr int kChunks = D / 64;              // boxes per 128-row tile
     static constexpr int kTileBytes = 128 * D * 2;
     static constexpr int kOffK = 0;
-    static constexpr int kOffV = kOffK + kTileBytes;
-    static constexpr int kOffDS = kOffV + kTileBytes;   // dS: 128 keys x 128 queries, MN-major
+    // dS: 128 keys x 128 queries, MN-major. At d = 64, V is read from shared memory only
+    // once, to copy it into TMEM before any dS is written, so it lands in the second dS
+    // buffer (which frees the room for a fourth ring stage).
+    static constexpr int kOffDS = kOffK + kTileBytes + (D == 64 ? 0 : kTileBytes);
+    static constexpr int kOffV = D == 64 ? kOffDS + 128 * 128 * 2 : kOffK + kTileBytes;
     // d = 64: a Q tile is two halves of 64 query columns, one per compute warpgroup, each
     // with its own S^T/dP^T commit and P^T/dS^T hand-off. S^T and dP^T of half h of the next
     // tile are issued right after dV and dK of half h of this one, before dQ, so one
