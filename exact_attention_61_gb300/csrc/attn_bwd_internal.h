@@ -16,6 +16,7 @@ struct BwdParams {
     const float* lse2;  // [BH][Npad] -LSE * log2(e); -inf on padded rows (P = 0 there)
     const float* dvec;  // [BH][Npad] -D = -rowsum(dO * O); 0 on padded rows
     float* dq_acc;      // [BH][N][d] fp32 sum of dS K over the key tiles (unscaled)
+    int* item_counter;  // persistent kernel: next work item to claim (zeroed by the prologue)
     void* dk;           // [BH][N][d] dtype
     void* dv;           // [BH][N][d] dtype
     uint32_t* err;      // device status record {code, block, where, iteration}
@@ -42,6 +43,7 @@ struct BwdPrepParams {
     float* lse2;        // [BH][Npad]
     float* dvec;        // [BH][Npad]
     float* dq_acc;      // [BH][N][d], zeroed here
+    int* item_counter;  // zeroed here
     int N, Npad, BH, d;  // N: query rows
 };
 

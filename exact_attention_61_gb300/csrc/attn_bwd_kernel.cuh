@@ -236,12 +236,14 @@ struct BwdCfg {
     static constexpr int kBarDqRead = kBarDqFull + 1;      // dQ tile read out
     static constexpr int kBarAcc = kBarDqRead + 1;         // dK, dV final
     static constexpr int kBarKvTmem = kBarAcc + 1;         // d = 64: K and V copied into TMEM
-    static constexpr int kBarDrain = kBarKvTmem + 1;
+    static constexpr int kBarAccFree = kBarKvTmem + 1;     // persistent form: dK, dV read out
+    static constexpr int kBarDrain = kBarAccFree + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     // The dynamic shared-memory base is 1024-byte aligned (declared so and checked at
-    // run time): d = 128 leaves no room for alignment slack.
-    static constexpr int kSmemBytes = kOffMisc + 16;
+    // run time): d = 128 leaves no room for alignment slack. misc: [0] TMEM base, [1] abort
+    // flag, [4..8) the persistent kernel's ring of claimed work items.
+    static constexpr int kSmemBytes = kOffMisc + 32;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     // TMEM columns: S^T/P^T, dP^T/dS^T, dV, dK, and the dQ tile (d = 128: over S^T).
     static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
@@ -708,6 +710,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams p) {
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = static_cast<int>(threadIdx.x & 31u);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.item_counter = 0;
     if (row >= static_cast<long long>(p.BH) * p.Npad) return;
     const int bh = static_cast<int>(row / p.Npad), i = static_cast<int>(row % p.Npad);
     const size_t vrow = static_cast<size_t>(bh) * p.Npad + i;

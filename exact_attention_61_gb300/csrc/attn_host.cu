@@ -466,7 +466,7 @@ int run_kv(void* ctx) {
 
 struct BwdLayout {
     int64_t Npad;
-    uint64_t lse2_off, dvec_off, dq_off, bytes;
+    uint64_t lse2_off, dvec_off, dq_off, counter_off, bytes;
 };
 
 BwdLayout bwd_layout(int64_t BH, int64_t N, int64_t d) {
@@ -475,7 +475,9 @@ BwdLayout bwd_layout(int64_t BH, int64_t N, int64_t d) {
     L.lse2_off = 0;
     L.dvec_off = static_cast<uint64_t>(BH) * L.Npad * 4u;
     L.dq_off = 2 * L.dvec_off;
-    L.bytes = L.dq_off + static_cast<uint64_t>(BH) * N * d * 4u;
+    // the persistent kernel's work-item counter (zeroed by the prologue)
+    L.counter_off = L.dq_off + static_cast<uint64_t>(BH) * N * d * 4u;
+    L.bytes = L.counter_off + 16u;
     return L;
 }
 
@@ -550,6 +552,7 @@ int bwd_impl(const BwdArgs& a) {
     float* lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
     float* dvec = reinterpret_cast<float*>(ws + L.dvec_off);
     float* dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
+    int* item_counter = reinterpret_cast<int*>(ws + L.counter_off);
     alignas(64) CUtensorMap maps[5];
     const void* ptrs[4] = {a.q, a.k, a.v, a.dout};
     const int64_t rows[4] = {a.Nq, a.Nk, a.Nk, a.Nq};
@@ -575,8 +578,8 @@ int bwd_impl(const BwdArgs& a) {
     const bool bf16 = a.dtype == ATTN_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(a.stream);
 
-    BwdPrepParams pp{a.o, a.dout, a.lse, lse2, dvec, dq_acc, static_cast<int>(a.Nq), static_cast<int>(L.Npad),
-                     static_cast<int>(BH), static_cast<int>(a.d)};
+    BwdPrepParams pp{a.o, a.dout, a.lse, lse2, dvec, dq_acc, item_counter, static_cast<int>(a.Nq),
+                     static_cast<int>(L.Npad), static_cast<int>(BH), static_cast<int>(a.d)};
     e = launch_bwd_prep(bf16, pp, s);
     if (e != cudaSuccess) return cuda_fail(e);
 
@@ -584,6 +587,7 @@ int bwd_impl(const BwdArgs& a) {
     p.lse2 = lse2;
     p.dvec = dvec;
     p.dq_acc = dq_acc;
+    p.item_counter = item_counter;
     p.dk = a.dk;
     p.dv = a.dv;
     p.err = status;

@@ -222,13 +222,16 @@ int attn_fwd_window_checked(const void* q, const void* k, const void* v, void* o
  *    [B, H, N] fp32 from attn_fwd with the same q, k, v, causal and scale.
  *  - dq, dk, dv: DEVICE [B, H, N, d] of `dtype`, written (rounded once from fp32).
  *  - workspace: DEVICE scratch owned by the caller, at least
- *    attn_bwd_workspace_bytes(B, H, N, d) bytes (fp32 D and LSE vectors and the
- *    dQ accumulator); nothing in it needs to be initialised. Calls that may run
- *    at the same time need workspaces of their own.
+ *    attn_bwd_workspace_bytes(B, H, N, d) bytes (fp32 D and LSE vectors, the dQ
+ *    accumulator and the counter of the d = 64 kernel's work items); nothing in it
+ *    needs to be initialised. Calls that may run at the same time need workspaces of
+ *    their own.
  *  - All ten pointers 16-byte aligned; the outputs and the workspace must not
  *    overlap each other or any input. Sizes and scale as for attn_fwd.
  *  - dQ is summed over key tiles with fp32 atomic additions, so its last bits
- *    may differ from run to run; dK and dV are deterministic.
+ *    may differ from run to run; dK and dV are deterministic (at d = 64 the key
+ *    tiles are handed to the CTAs in the order they ask, which changes only the
+ *    order of those dQ additions).
  *  - Returns ATTN_OK once the three kernels are enqueued, or an error status
  *    with nothing enqueued (ATTN_ERR_INVALID_ARG also for a short workspace).
  */
@@ -272,7 +275,8 @@ int attn_bwd_window_checked(const void* q, const void* k, const void* v, const v
 
 /* attn_bwd_workspace_bytes -- workspace attn_bwd needs for these sizes (N = the query
  * rows; for attn_bwd_window pass Nq): 8 bytes per row padded to 128 rows, plus 4*d
- * bytes per row (0 for sizes attn_bwd rejects). Pure host arithmetic, no CUDA call. */
+ * bytes per row, plus 16 bytes (a work-item counter) (0 for sizes attn_bwd rejects).
+ * Pure host arithmetic, no CUDA call. */
 size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
 /*

@@ -221,8 +221,9 @@ def test_bwd_host_validation(lib, kw, status):
 def test_bwd_workspace_bytes(lib):
     from exact_attention_61_gb300 import attn
     # 8 bytes per row padded to 128 rows (LSE, D) + 4 d bytes per row (dQ accumulator)
-    assert attn.bwd_workspace_bytes(1, 2, 300, 64) == 2 * 384 * 8 + 2 * 300 * 64 * 4
-    assert attn.bwd_workspace_bytes(4, 16, 4096, 128) == 64 * 4096 * 8 + 64 * 4096 * 128 * 4
+    # D and LSE vectors (rows padded to 128), the fp32 dQ accumulator, a 16-byte work counter
+    assert attn.bwd_workspace_bytes(1, 2, 300, 64) == 2 * 384 * 8 + 2 * 300 * 64 * 4 + 16
+    assert attn.bwd_workspace_bytes(4, 16, 4096, 128) == 64 * 4096 * 8 + 64 * 4096 * 128 * 4 + 16
     assert attn.bwd_workspace_bytes(1, 1, 1, 96) == 0
     assert attn.bwd_workspace_bytes(0, 1, 128, 64) == 0
 
