@@ -7,7 +7,7 @@ namespace attn_sm103 {
 
 cudaError_t launch_bwd_prep(bool bf16, const BwdPrepParams& p, cudaStream_t s) {
     const long long rows = static_cast<long long>(p.BH) * p.Npad;
-    const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+    const unsigned blocks = static_cast<unsigned>((rows * (p.d / 8) + 255) / 256);
     if (bf16)
         attn_bwd_prep_kernel<true><<<blocks, 256, 0, s>>>(p);
     else

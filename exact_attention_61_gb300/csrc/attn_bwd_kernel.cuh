@@ -704,44 +704,46 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 }
 
 // -D_i = -rowsum(dO * O), -lse2_i = -LSE_i log2(e) (-inf where LSE = -inf or i >= N, so
-// that P = 0 there), and the zeroed dQ accumulator. One warp per row of [BH][Npad]. The
-// main kernel adds them, so they are stored negated.
+// that P = 0 there), the zeroed dQ accumulator and the persistent kernel's zeroed work
+// counter. Each thread takes 8 consecutive elements (16 bytes of O and of dO, 32 bytes of
+// the accumulator) of one row of [BH][Npad], d/8 threads per row summed by shuffles. The
+// main kernel adds the vectors, so they are stored negated.
 template <bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams p) {
-    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = static_cast<int>(threadIdx.x & 31u);
+    const int tpr = p.d / 8;  // threads per row: 8 or 16, a divisor of the warp
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long row = t / tpr;
+    const int sub = static_cast<int>(t % tpr);
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.item_counter = 0;
-    if (row >= static_cast<long long>(p.BH) * p.Npad) return;
-    const int bh = static_cast<int>(row / p.Npad), i = static_cast<int>(row % p.Npad);
-    const size_t vrow = static_cast<size_t>(bh) * p.Npad + i;
-    if (i >= p.N) {
-        if (lane == 0) {
+    const bool valid = row < static_cast<long long>(p.BH) * p.Npad;
+    const int bh = valid ? static_cast<int>(row / p.Npad) : 0, i = valid ? static_cast<int>(row % p.Npad) : 0;
+    float acc = 0.f;
+    if (valid && i < p.N) {
+        const size_t off = (static_cast<size_t>(bh) * p.N + i) * p.d + sub * 8;
+        const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + off);
+        const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + off);
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 a = unpack2<BF16>(ow[e]), b = unpack2<BF16>(gw[e]);
+            acc = fmaf(a.x, b.x, acc);
+            acc = fmaf(a.y, b.y, acc);
+        }
+        float4* z = reinterpret_cast<float4*>(p.dq_acc + off);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int w = tpr / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (valid && sub == 0) {
+        const size_t vrow = static_cast<size_t>(bh) * p.Npad + i;
+        if (i >= p.N) {
             p.lse2[vrow] = -INFINITY;
             p.dvec[vrow] = -0.f;
-        }
-        return;
-    }
-    const size_t off = (static_cast<size_t>(bh) * p.N + i) * p.d;
-    const int per = p.d / 32;  // 2 or 4 elements per lane
-    float acc = 0.f;
-    for (int e = 0; e < per; ++e) {
-        float o, g;
-        if constexpr (BF16) {
-            o = __bfloat162float(static_cast<const __nv_bfloat16*>(p.o)[off + lane * per + e]);
-            g = __bfloat162float(static_cast<const __nv_bfloat16*>(p.dout)[off + lane * per + e]);
         } else {
-            o = __half2float(static_cast<const __half*>(p.o)[off + lane * per + e]);
-            g = __half2float(static_cast<const __half*>(p.dout)[off + lane * per + e]);
+            const float l = p.lse[static_cast<size_t>(bh) * p.N + i];
+            p.lse2[vrow] = l == -INFINITY ? -INFINITY : -(l * 1.4426950408889634f);
+            p.dvec[vrow] = -acc;
         }
-        acc = fmaf(o, g, acc);
-        p.dq_acc[off + lane * per + e] = 0.f;
-    }
-#pragma unroll
-    for (int w = 16; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (lane == 0) {
-        const float l = p.lse[static_cast<size_t>(bh) * p.N + i];
-        p.lse2[vrow] = l == -INFINITY ? -INFINITY : -(l * 1.4426950408889634f);
-        p.dvec[vrow] = -acc;
     }
 }
 
