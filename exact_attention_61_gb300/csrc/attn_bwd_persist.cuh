@@ -7,10 +7,9 @@
 // tile sees from 1 to all Q tiles), and a static assignment left some SMs 15 % more work
 // than the average. Non-causal items are all alike and go round-robin (item k of CTA c is
 // c + k * gridDim.x). The loader picks the next item once the current one's copies are
-// issued, and passes each item to the other roles
-// through a ring of four slots in shared memory, written before the loader's arrive on
-// the K/V barrier of that item; an item past the list is passed on as -1 and ends every
-// role.
+// issued, and passes each item to the other roles through a ring of four slots in shared
+// memory, written before the loader's arrive on the K/V barrier of that item; an item
+// past the list is passed on as -1 and ends every role.
 //
 // Per item it computes what attn_bwd_kernel computes at d = 64, with the same arithmetic
 // in the same order (the dQ accumulator receives the same tiles; only the order in which
