@@ -168,3 +168,26 @@ def test_sum_rules_hold_on_the_gpu(cuda_lib):
     dvs = dv.double().sum(dim=2)
     dos = do.double().sum(dim=2)
     assert ((dvs - dos).abs() / dv.double().abs().sum(dim=2)).max().item() < 3e-2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_headline_size_every_head_identities(cuda_lib, causal):
+    """B=4, H=16, N=4096, d=64, bf16 (the persistent d=64 backward: 2048 key-tile items over
+    the SMs; causal items claimed from a counter). Every head satisfies
+    sum_j dK_j = 0, sum_j dV_j = sum_i dO_i, and sum_i q_i . dQ_i = sum_j k_j . dK_j (scaling
+    Q or K scales the scores alike). The last ties dQ, summed over every key-tile item of
+    the head, to dK: an item whose dQ is lost or added twice breaks it."""
+    B, H, N, d = 4, 16, 4096, 64
+    q, k, v, do = (t.cuda() for t in _inputs(B, H, N, d, "bf16", seed=62800 + int(causal)))
+    o, lse = cuda_lib.fwd(q, k, v, causal=causal, checked=True)
+    dq, dk, dv = cuda_lib.bwd(q, k, v, o, lse, do, causal=causal, checked=True)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    dk64, dv64, dq64 = dk.double(), dv.double(), dq.double()
+    rel = lambda a, b, s: ((a - b).abs() / s.clamp_min(1e-30)).max().item()
+    assert rel(dk64.sum(dim=2), 0.0, dk64.abs().sum(dim=2)) < 3e-2
+    assert rel(dv64.sum(dim=2), do.double().sum(dim=2), dv64.abs().sum(dim=2)) < 3e-2
+    qdq = q.double() * dq64
+    kdk = k.double() * dk64
+    assert rel(qdq.sum(dim=(2, 3)), kdk.sum(dim=(2, 3)), qdq.abs().sum(dim=(2, 3)) + kdk.abs().sum(dim=(2, 3))) < 5e-3
