@@ -9,8 +9,9 @@ convention of the profile-driven FlashAttention-2 page (Round 0 / Step 5).
 Timing: W warm-up steps (plus enough extra steps to keep the GPU busy for
 --warmup-seconds, so clocks have ramped), peak-memory counters reset after
 warm-up, then K steps timed with CUDA events on the launching stream, the L2
-cache flushed (a write of twice its size) before every step outside the events,
-a barrier and a synchronize on both sides of the timed region, max over ranks.
+cache flushed before every step outside the events (a write of twice its size,
+then a read of another buffer of twice its size, so that the write's dirty lines
+go back to HBM before the step rather than inside it), a barrier and a synchronize on both sides of the timed region, max over ranks.
 `value`, `ms_per_step` and `roofline.achieved` come from the per-step medians
 (the means, p10 and p90 are reported beside them).
 
@@ -322,6 +323,31 @@ def rank_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+L2_NOTE = ("flushed before every step outside the events: a write of 2x L2 size, then a read of "
+           "another 2x L2 buffer that writes the dirty lines back before the step")
+
+
+class L2Flush:
+    """Evicts a step's inputs from L2 between steps, outside the timed region.
+
+    A write of twice the L2 size evicts every input line but leaves L2 full of dirty
+    lines, which the next step would then write back to HBM inside its own timed
+    region (about 126 MB: 9-12 % of an HBM-bound decode step). A read of a second
+    buffer of twice the L2 size afterwards writes them back first, so the step starts
+    from a cold, clean L2 as the first step after a read-only phase would.
+    ``write_only=True`` keeps the bare write, for the comparison figure."""
+
+    def __init__(self, torch, dev, l2: int):
+        n = 2 * max(l2, 64 << 20)
+        self.w = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(n // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self, i: int, write_only: bool = False):
+        self.w.fill_(i & 0xFF)
+        if not write_only:
+            self.r.sum()
+
+
 def run_reference(args) -> int:
     rank, _, world = rank_env()
     if rank != 0:
@@ -384,7 +410,7 @@ def run_ours(args) -> int:
     sptr = stream.cuda_stream
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, l2)
     dt = attn.ATTN_BF16
 
     def launch(causal, q_=q, k_=k, v_=v, o_=None, l_=None, shape=(B, H, N, D)):
@@ -400,7 +426,7 @@ def run_ours(args) -> int:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
         for i in range(n):
             if flush_l2:
-                flush.fill_(i & 0xFF)
+                flush(i)
             ev[i][0].record(stream)
             launch(False)
             ev[i][1].record(stream)
@@ -415,7 +441,7 @@ def run_ours(args) -> int:
     t_w = time.perf_counter()
     n_warm = 0
     while n_warm < args.warmup or time.perf_counter() - t_w < args.warmup_seconds:
-        flush.fill_(n_warm & 0xFF)
+        flush(n_warm)
         launch(False)
         launch(True)
         n_warm += 1
@@ -452,7 +478,7 @@ def run_ours(args) -> int:
         os_, ls_ = torch.empty_like(qs), torch.empty((b_, h_, n_), dtype=torch.float32, device=dev)
         ts = []
         for i in range(max(3, args.warmup) + args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             launch(causal, qs, ks, vs, os_, ls_, (b_, h_, n_, d_))
@@ -541,7 +567,7 @@ def run_ours(args) -> int:
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "scale": scale,
                        "causal": [False, True], "seed": SEED,
-                       "l2": "flushed before every step (write of 2x L2 size, outside the events)",
+                       "l2": L2_NOTE,
                        "statistic": "median over the timed steps (mean, p10, p90 in per_kernel)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "per_kernel": {
@@ -617,7 +643,7 @@ def run_decode(args) -> int:
     scale = 1.0 / math.sqrt(w.d)
     dt = attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_FP16
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, l2)
 
     def launch():
         st = attn.attn_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
@@ -630,25 +656,40 @@ def run_decode(args) -> int:
     t_w = time.perf_counter()
     n_warm = 0
     while n_warm < args.warmup or time.perf_counter() - t_w < args.warmup_seconds:
-        flush.fill_(n_warm & 0xFF)
+        flush(n_warm)
         launch()
         n_warm += 1
         if n_warm % 16 == 0:
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    def timed(n, write_only=False):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            flush(i, write_only)
+            ev[i][0].record(stream)
+            launch()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [e0.elapsed_time(e1) for e0, e1 in ev]
+
     t0 = time.time()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        launch()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    t_ms = timed(args.steps)
     t1 = time.time()
     if sampler:
         sampler.stop()
-    t_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    ms = statistics.fmean(t_ms)
+    # outside the timed region: the same steps after a bare write flush (its dirty lines are
+    # written back inside each step), and back to back without a flush
+    t_wo = timed(args.steps, write_only=True)
+    t_nf = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        t_nf.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    t_nf = [a.elapsed_time(b) for a, b in t_nf]
+    ms = statistics.median(t_ms)
     nbytes = decode_bytes(w.B, w.H, w.Nq, w.Nk, w.d)
     gbs = nbytes / (ms * 1e-3) / 1e9
     peaks = measured_peaks()
@@ -660,8 +701,8 @@ def run_decode(args) -> int:
         "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
                    "mask": "causal_bottom_right", "key_splits": splits, "seed": w.seed,
-                   "l2": "flushed before every step (write of 2x L2 size, outside the events)"},
-        "ms_median": statistics.median(t_ms), "ms_p10": _pct(t_ms, 10), "ms_p90": _pct(t_ms, 90),
+                   "l2": L2_NOTE, "statistic": "median over the timed steps"},
+        "ms_mean": statistics.fmean(t_ms), "ms_p10": _pct(t_ms, 10), "ms_p90": _pct(t_ms, 90),
         "roofline": {"bound": "hbm", "kernel": "attn_decode_kernel + attn_merge_kernel (one call)",
                      "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": None,
@@ -669,6 +710,13 @@ def run_decode(args) -> int:
                      "peak_source": "measured copy (MEASURED_PEAKS.json)"
                      if peaks["source"] == "measured" else "fallback 6.8 TB/s"},
         "gpu_launches": (2 if ws_n else 1) * args.steps,
+        "l2_write_flush_only": {"ms_median": statistics.median(t_wo),
+                                "gbs": nbytes / (statistics.median(t_wo) * 1e-3) / 1e9,
+                                "note": "the same steps after a bare 2x L2 write, whose dirty lines "
+                                        "are written back inside each step"},
+        "no_l2_flush": {"ms_median": statistics.median(t_nf),
+                        "gbs": nbytes / (statistics.median(t_nf) * 1e-3) / 1e9,
+                        "note": "the same steps back to back (K and V are larger than L2)"},
     }
     if sampler:
         out["clocks"] = summarize_clocks(sampler.samples, t0 - args.warmup_seconds, t1)
@@ -707,7 +755,7 @@ def run_bwd(args) -> int:
     ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, l2)
 
     def launch(causal):
         o, lse = outs[causal]
@@ -721,7 +769,7 @@ def run_bwd(args) -> int:
     t_w = time.perf_counter()
     n_warm = 0
     while n_warm < args.warmup or time.perf_counter() - t_w < args.warmup_seconds:
-        flush.fill_(n_warm & 0xFF)
+        flush(n_warm)
         launch(False)
         launch(True)
         n_warm += 1
@@ -731,7 +779,7 @@ def run_bwd(args) -> int:
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0 = time.time()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(stream)
         launch(False)
         ev[i][1].record(stream)
@@ -743,7 +791,7 @@ def run_bwd(args) -> int:
         sampler.stop()
     t_nc = [e[0].elapsed_time(e[1]) for e in ev]
     t_c = [e[1].elapsed_time(e[2]) for e in ev]
-    ms_nc, ms_c = statistics.fmean(t_nc), statistics.fmean(t_c)
+    ms_nc, ms_c = statistics.median(t_nc), statistics.median(t_c)
     f_nc, f_c = bwd_flops(B, H, N, D, False), bwd_flops(B, H, N, D, True)
     peaks = measured_peaks()
     ach = tflops(f_nc, ms_nc)
@@ -754,10 +802,10 @@ def run_bwd(args) -> int:
         "config": {"workload": f"b{B}h{H}n{N}d{D} bf16 backward, non-causal + causal per step", "B": B, "H": H,
                    "N": N, "d": D, "scale": scale, "seed": SEED,
                    "flops": "10 B H N^2 d (five N x N x d products), halved for causal",
-                   "l2": "flushed before every step (write of 2x L2 size, outside the events)"},
-        "per_kernel": {"noncausal": {"ms_mean": ms_nc, "ms_median": statistics.median(t_nc),
+                   "l2": L2_NOTE, "statistic": "median over the timed steps"},
+        "per_kernel": {"noncausal": {"ms_median": ms_nc, "ms_mean": statistics.fmean(t_nc),
                                      "tflops": tflops(f_nc, ms_nc)},
-                       "causal": {"ms_mean": ms_c, "ms_median": statistics.median(t_c),
+                       "causal": {"ms_median": ms_c, "ms_mean": statistics.fmean(t_c),
                                   "tflops": tflops(f_c, ms_c)}},
         "roofline": {"bound": "tensor", "kernel": "attn_bwd (prep + attn_bwd_kernel + dQ cast), non-causal",
                      "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -787,7 +835,7 @@ def run_fwd_shapes(args) -> int:
     attn.load()
     peaks = measured_peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, l2)
     stream = torch.cuda.current_stream(dev)
     for spec in args.fwd_shapes.split(";"):
         b_, h_, n_, d_ = (int(x) for x in spec.split(","))
@@ -803,24 +851,24 @@ def run_fwd_shapes(args) -> int:
                 if st != attn.ATTN_OK:
                     raise RuntimeError(f"attn_fwd failed: {attn.strerror(st)}")
             for i in range(max(args.warmup, 3)):
-                flush.fill_(i & 0xFF)
+                flush(i)
                 launch()
             ts = []
             for i in range(args.steps):
-                flush.fill_(i & 0xFF)
+                flush(i)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 launch()
                 e1.record(stream)
                 ts.append((e0, e1))
             torch.cuda.synchronize(dev)
-            ms = statistics.fmean(a.elapsed_time(b) for a, b in ts)
+            ms = statistics.median(a.elapsed_time(b) for a, b in ts)
             f = counts.attn_flops(b_, h_, n_, d_, causal)
-            res["causal" if causal else "noncausal"] = {"ms_mean": ms, "tflops": tflops(f, ms),
+            res["causal" if causal else "noncausal"] = {"ms_median": ms, "tflops": tflops(f, ms),
                                                         "frac_of_peak": tflops(f, ms) / peaks["bf16_tflops"]}
         print(json.dumps({"metric": f"attention fwd TFLOP/s at B={b_},H={h_},N={n_},d={d_} bf16",
                           "unit": "TFLOP/s", "steps": args.steps, "dtype": "bf16", "data": "synthetic",
-                          "l2": "flushed before every launch", **res}), flush=True)
+                          "l2": L2_NOTE, **res}), flush=True)
         del q, k, v, o, lse
     return 0
 
