@@ -340,7 +340,7 @@ class L2Flush:
     def __init__(self, torch, dev, l2: int):
         n = 2 * max(l2, 64 << 20)
         self.w = torch.empty(n, dtype=torch.uint8, device=dev)
-        self.r = torch.zeros(n // 4, dtype=torch.int32, device=dev)
+        self.r = torch.zeros(n // 4, dtype=torch.float32, device=dev)  # summed in place, no copy
 
     def __call__(self, i: int, write_only: bool = False):
         self.w.fill_(i & 0xFF)
