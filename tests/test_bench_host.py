@@ -1,6 +1,6 @@
 """Host logic of bench.py, on the CPU: throughput aggregation, the max-over-ranks
 reduction across two gloo ranks, clock summaries, the ncu-traffic bookkeeping and
-the reference (oracle) arm's JSON line."""
+the reference (oracle) arm's JSON line, and the L2 flush helper."""
 import json
 import os
 import socket
@@ -164,3 +164,33 @@ def test_spot_check_flags_errors():
     assert not r["ok"] and r["over_tol_o"] == 1 and r["max_abs_err_o"] == pytest.approx(0.05)
     r = bench.spot_check(o_ref, l_ref + 2e-3, o_ref, l_ref)
     assert not r["ok"] and r["over_tol_lse"] == 8
+
+
+def test_l2_flush_writes_then_reads_without_a_copy():
+    """The flush writes a buffer of twice the L2 size (64 MB at least), then sums a float32
+    buffer of the same size: float32 sums in place, with no widening copy (an int32 buffer
+    would first be copied to int64, a second large write)."""
+    import torch
+    calls = []
+
+    class Spy(torch.Tensor):
+        pass
+
+    f = bench.L2Flush(torch, "cpu", 1 << 20)
+    n = 2 * (64 << 20)
+    assert f.w.numel() == n and f.w.dtype == torch.uint8
+    assert f.r.numel() * f.r.element_size() == n and f.r.dtype == torch.float32
+    assert f.r.sum().dtype == torch.float32  # no promotion, so no widening copy
+    orig = f.r
+    f.r = orig.as_subclass(Spy)
+    torch_sum = Spy.sum
+
+    def spy_sum(self, *a, **k):
+        calls.append(1)
+        return torch_sum(self, *a, **k)
+
+    Spy.sum = spy_sum
+    f(7)
+    assert int(f.w[0]) == 7 and int(f.w[-1]) == 7 and calls == [1]
+    f(8, write_only=True)
+    assert int(f.w[0]) == 8 and calls == [1]
