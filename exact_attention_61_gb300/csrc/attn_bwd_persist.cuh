@@ -15,22 +15,26 @@
 // in the same order (the dQ accumulator receives the same tiles; only the order in which
 // the CTAs add them differs, as between any two launches): the FlashAttention-2 backward
 // that "如何用 profiler 逐步优化 Triton FlashAttention-2 kernel" ("Future articles") names,
-// from the L the forward writes ("Round 4 / exp2"). The roles are those of the one-item
-// kernel:
+// from the L the forward writes ("Round 4 / exp2"). The roles:
 //  - warps 0-7: two compute warpgroups, one per 64-query half of each Q tile;
-//  - warps 8-11: copy K and V into TMEM at the start of each item, read each dQ tile out
-//    and add it to the fp32 accumulator by TMA reduce-add;
-//  - warp 12 issues the MMAs, warp 13 drives TMA.
+//  - warps 8-11: read each dQ tile out and add it to the fp32 accumulator by TMA
+//    reduce-add;
+//  - warp 12 issues the MMAs and, at the start of each item, the copies of K and V into
+//    TMEM (tcgen05.cp); warp 13 drives TMA.
 // Every barrier that paces Q tiles counts the CTA's Q tiles over all its items; the ones
-// that pace items (K/V landed, K/V in TMEM, dK/dV final, dK/dV read out) count items.
+// that pace items (K/V landed, item read by the dQ warps, dK/dV final, dK/dV read out)
+// count items.
 // Across an item boundary:
 //  - the loader reloads K and V (shared memory) once every MMA of the previous item is
 //    done (kBarAcc), since the last dQ products read K there and V shares the second dS
-//    buffer; the dQ warps then copy them into TMEM (the previous item's S^T/dP^T, which
-//    read the TMEM copies, are done too);
-//  - the MMA warp issues the new item's first S^T/dP^T as soon as K and V are in TMEM,
-//    and its first dV/dK (which overwrite the accumulators) only after the compute
-//    warpgroups have read the previous item's dV and dK out (kBarAccFree).
+//    buffer;
+//  - once they land, the MMA warp copies them into TMEM (the previous item's S^T/dP^T,
+//    which read the old copies, are done too) and issues the new item's first S^T/dP^T
+//    behind the copies; the compute warpgroups write dS over V's shared memory only after
+//    those S^T/dP^T completed, and so after the copy of V;
+//  - the MMA warp issues the item's first dV/dK (which overwrite the accumulators) only
+//    after the compute warpgroups have read the previous item's dV and dK out
+//    (kBarAccFree).
 // Every wait is bounded as in the other kernels.
 #pragma once
 
@@ -62,6 +66,9 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
     using C = BwdCfg<64>;
     constexpr int D = 64;
     static_assert(C::kEarlyNext && C::kKvTmem, "the persistent kernel is the d = 64 form");
+    // The one-item kernel's K/V-in-TMEM barrier; here the dQ warps arrive on it once they
+    // have read item k from the ring (they have passed their wait on the K/V barrier).
+    constexpr int kBarDqItem = C::kBarKvTmem;
     extern __shared__ __align__(1024) uint8_t smem_bwd[];
     const uint32_t base = smem_addr(smem_bwd);
     if (base & 1023u) {  // uniform over the CTA: nothing has been set up yet
@@ -89,7 +96,7 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
             uint32_t count = 1;
             if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages) count = 1 + 8 + 1;  // MMA, compute, dQ store
             if (i == C::kBarPds || i == C::kBarPds + 1) count = 4;                         // a compute warpgroup
-            if (i == C::kBarDqRead || i == C::kBarKvTmem) count = 4;                       // dQ warps
+            if (i == C::kBarDqRead || i == kBarDqItem) count = 4;                          // dQ warps
             if (i == C::kBarAccFree) count = 8;                                            // compute warps
             mbar_init(bar(i), count);
         }
@@ -131,11 +138,16 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
             for (;; ++k) {
                 const int x = x_next;
                 items[k & 3] = x;
+                // Before the K/V barrier's next phase, every role has passed its wait on the
+                // previous one: the MMA and compute warps, since every MMA of the previous item
+                // is done (kBarAcc); the dQ warps by their own arrive (with one-tile items the
+                // MMAs can finish while the dQ warps are still on the item before). Then no
+                // role's parity wait can fall two phases behind.
+                if (k > 0 && !wait_one(bar(kBarDqItem), (k - 1) & 1, wc, kRoleBwdLoad * 1000 + 93, k)) break;
                 if (x < 0) {
                     // No more items: complete the K/V barrier's next phase with no bytes so that
                     // the other roles read the -1. As for an item, only once every MMA of the
-                    // previous item is done: then its copy has landed and every role has passed
-                    // its phase, so no role's parity wait can fall two phases behind.
+                    // previous item is done (its copy has landed).
                     if (k > 0 && !wait_one(bar(C::kBarAcc), (k - 1) & 1, wc, kRoleBwdLoad * 1000 + 92, k)) break;
                     last_kv = -1;
                     mbar_arrive(bar(C::kBarKV));
@@ -210,10 +222,12 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
             return true;
         };
 
+        const uint64_t dK_cp = sdesc_sw128(base + C::kOffK, 16, 1024);  // K, V as K-major copy sources
+        const uint64_t dV_cp = sdesc_sw128(base + C::kOffV, 16, 1024);
         bool ok = true;
         int gi = 0;  // Q tiles issued so far (all items)
         for (int k = 0; ok; ++k) {
-            ok = wait_warp_sleep(bar(C::kBarKvTmem), k & 1, wc, kRoleBwdMma * 1000 + C::kBarKvTmem, k);
+            ok = wait_warp_sleep(bar(C::kBarKV), k & 1, wc, kRoleBwdMma * 1000 + C::kBarKV, k);
             if (!ok) break;
             const int x = items[k & 3];
             if (x < 0) break;
@@ -221,6 +235,11 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
             bwd_persist_item<CAUSAL>(x, p, bh, kt);
             const int n_it = n_qt - q_begin(kt);
             tc_fence_after_sync();
+            // K and V into TMEM, the A operands of S^T and dP^T. The previous item's MMAs,
+            // which read the old copies, are complete: the loader reloaded K and V only
+            // after its kBarAcc.
+            tmem_cp_tile64_warp(tmem + C::colK, dK_cp);
+            tmem_cp_tile64_warp(tmem + C::colV, dV_cp);
             ok = issue_sdp_half(gi, 0) && issue_sdp_half(gi, 1);
             for (int it = 0; it < n_it && ok; ++it, ++gi) {
                 const int s = gi % C::kStages;
@@ -256,7 +275,7 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
         wait_warp(bar(C::kBarDrain), 0, wc, kRoleBwdMma * 1000 + C::kBarDrain, 0, false);
         __syncwarp();
     } else if (warp >= C::kWarpDq) {
-        // ================================ K/V copy, dQ read-out =======================
+        // ================================ dQ read-out and reduce ======================
         const uint32_t wq = warp - C::kWarpDq;
         const uint32_t r = wq * 32u + lane;
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
@@ -268,33 +287,13 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
             ok = wait_warp_sleep(bar(C::kBarKV), k & 1, wc, kRoleBwdDq * 1000 + C::kBarKV, k);
             if (!ok) break;
             const int x = items[k & 3];
-            if (x < 0) {  // no more items: pass the -1 on to the MMA and compute warps
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::kBarKvTmem));
-                break;
-            }
+            if (x < 0) break;  // no more items
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarDqItem));
             int bh, kt;
             bwd_persist_item<CAUSAL>(x, p, bh, kt);
             const int qt0 = q_begin(kt);
             const int n_it = n_qt - qt0;
-            // K and V rows (128-byte-swizzled in shared memory) into TMEM lane r, 16-bit
-            // pairs per column: the A operands of S^T and dP^T.
-            {
-#pragma unroll 1
-                for (int m = 0; m < 2; ++m) {
-                    const uint32_t row = base + (m ? C::kOffV : C::kOffK) + r * 128u;
-                    uint32_t xr[32];
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        ld_shared_v4(row + ((ch ^ (r & 7u)) << 4), xr[4 * ch], xr[4 * ch + 1], xr[4 * ch + 2],
-                                     xr[4 * ch + 3]);
-                    tmem_st32(lane_base + (m ? C::colV : C::colK), xr);
-                }
-                tmem_st_wait();
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarKvTmem));
             for (int it = 0; it < n_it; ++it, ++gi) {
                 if (!wait_warp_sleep(bar(C::kBarDqFull), gi & 1, wc, kRoleBwdDq * 1000 + C::kBarDqFull, gi)) {
                     ok = false;
@@ -348,8 +347,8 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
         bool ok = true;
         int gi = 0;
         for (int k = 0; ok; ++k) {
-            // the item (or the -1 that ends the list), passed on by the K/V copy in TMEM
-            ok = wait_warp_sleep(bar(C::kBarKvTmem), k & 1, wc, kRoleBwdCompute * 1000 + C::kBarKvTmem, k);
+            // the item (or the -1 that ends the list), written before the K/V barrier's arrive
+            ok = wait_warp_sleep(bar(C::kBarKV), k & 1, wc, kRoleBwdCompute * 1000 + C::kBarKV, k);
             if (!ok) break;
             const int x = items[k & 3];
             if (x < 0) break;

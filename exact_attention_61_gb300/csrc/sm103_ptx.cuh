@@ -268,6 +268,28 @@ __device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
+// A 128-row, 64-element 16-bit tile, K-major in one 128-byte-swizzled box (the descriptor
+// of its first 16 elements, as for an MMA operand), copied into TMEM: row i to lane i of
+// `taddr`, element pairs in consecutive 32-bit columns (32 columns), i.e. the layout of an
+// A operand that an MMA reads from TMEM. Four tcgen05.cp of 128 rows x 256 bits, each 16
+// elements further (32 bytes: 2 units of the start-address field) and 8 columns further.
+// Warp-wide; elect.sync picks the issuing lane. Like an MMA the copy is asynchronous: the
+// MMAs this thread issues after it see its result, and a later tcgen05.commit tracks it.
+__device__ __forceinline__ void tmem_cp_tile64_warp(uint32_t taddr, uint64_t sdesc) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 ta;\n\t.reg .b64 sd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t"
+        "add.u32 ta, %0, 8;\n\tadd.u64 sd, %1, 2;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [ta], sd;\n\t"
+        "add.u32 ta, %0, 16;\n\tadd.u64 sd, %1, 4;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [ta], sd;\n\t"
+        "add.u32 ta, %0, 24;\n\tadd.u64 sd, %1, 6;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [ta], sd;\n\t}" ::"r"(taddr),
+        "l"(sdesc)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"

@@ -3,18 +3,19 @@
 A model of `exact_attention_61_gb300/csrc/attn_bwd_persist.cuh`. One CTA's roles run as
 coroutines over mbarriers with the hardware's parity-wait rule:
 - the loader: K/V per item, the Q/dO ring per Q tile, an end-of-list hand-off;
-- the dQ warps: the K/V copy into TMEM per item, and the dQ read-out and reduce per Q tile;
-- the MMA warp;
+- the dQ warps: an acknowledgement per item, the dQ read-out and reduce per Q tile;
+- the MMA warp: per item the K/V copy into TMEM (tcgen05.cp), then the MMAs;
 - the two compute warpgroups, one per 64-query half.
 
-The tensor core executes the MMA warp's operations in issue order. Copies land after random
-delays, and the roles advance at random. Over many random schedules and item lists the model
+The tensor core executes the MMA warp's copies and MMAs in issue order. Copies land after
+random delays, and the roles advance at random. Over many random schedules and item lists the model
 checks three things:
 
 1. every parity wait is exact: when it polls, the barrier has completed either the phase
    it waits for or the one before it;
 2. no data hazard. S^T/dP^T never overwrite P^T/dS^T that dV/dK still have to read. K/V in
-   TMEM are rewritten only after the previous item's S^T/dP^T executed. K and V in shared
+   TMEM are copied over only once the previous item's S^T/dP^T executed (checked when the
+   copy is issued, not only when it runs). K and V in shared
    memory are reloaded only after every reader is done; V shares the second dS buffer. A dS
    buffer is rewritten only after the dQ that read it. The dQ columns are overwritten only
    after they were read out. The accumulators are overwritten only after the previous
@@ -69,7 +70,7 @@ class Model:
         self.dq_full = B("dq_full")
         self.dq_read = B("dq_read")
         self.acc = B("acc")
-        self.kv_tmem = B("kv_tmem")
+        self.dq_item = B("dq_item")  # the dQ warps read item k (passed their K/V wait)
         self.acc_free = B("acc_free", 2)
         self.queue = []  # tensor core FIFO: ("mma", fn) / ("commit", bar)
         self.tma = []    # copies in flight
@@ -128,6 +129,8 @@ class Model:
     def loader(self):
         gi = 0
         for k, n_it in enumerate(self.items):
+            if k > 0 and self.plant != "loader_no_dq_item_wait":
+                yield from self.wait(self.dq_item, k - 1)
             if n_it < 0:  # end of the list: complete the K/V barrier's next phase with no bytes
                 if k > 0:
                     if self.plant == "end_waits_kv_only":
@@ -173,16 +176,8 @@ class Model:
         for k, n_it in enumerate(self.items):
             yield from self.wait(self.kv, k)
             if n_it < 0:
-                self.kv_tmem.arrive()
                 return
-            if self.smem_kv != k:
-                raise HazardError(f"K/V copy of item {k} reads shared memory holding item {self.smem_kv}")
-            if self.sdp_reads_kv.get(k - 1, 0):
-                raise HazardError(f"K/V of item {k} copied into TMEM while S^T/dP^T of item {k - 1} read it")
-            self.tmem_kv = k
-            self.v_copied.add(k)
-            self.kv_tmem.arrive()
-            yield
+            self.dq_item.arrive()
             for _ in range(n_it):
                 yield from self.wait(self.dq_full, gi)
                 if self.dq_tmem != ("dq", gi):
@@ -217,9 +212,24 @@ class Model:
             self.commit(self.sdp[h])
 
         for k, n_it in enumerate(self.items):
-            yield from self.wait(self.kv_tmem, k)
+            if self.plant != "mma_cp_before_kv_wait":
+                yield from self.wait(self.kv, k)
             if n_it < 0:
+                if self.plant == "mma_cp_before_kv_wait":
+                    yield from self.wait(self.kv, k)
                 return
+            # the K/V copy into TMEM, queued ahead of the item's MMAs
+            if self.sdp_reads_kv.get(k - 1, 0):
+                raise HazardError(f"K/V of item {k} copied into TMEM while S^T/dP^T of item {k - 1} read it")
+
+            def cp(k=k):
+                if self.smem_kv != k:
+                    raise HazardError(f"K/V copy of item {k} read shared memory holding item {self.smem_kv}")
+                self.tmem_kv = k
+                self.v_copied.add(k)
+            self.issue(cp)
+            if self.plant == "mma_cp_before_kv_wait":
+                yield from self.wait(self.kv, k)
             for h in range(2):
                 if h == 0:
                     yield from self.wait(self.qd_full[gi % ST], gi // ST)
@@ -284,7 +294,7 @@ class Model:
     def compute(self, h):
         gi = 0
         for k, n_it in enumerate(self.items):
-            yield from self.wait(self.kv_tmem, k)
+            yield from self.wait(self.kv, k)
             if n_it < 0:
                 return
             for _ in range(n_it):
@@ -370,17 +380,22 @@ def test_persistent_backward_headline_items():
     Model([32, 24, 17, 11, 6, 2, 1, -1], rng).run(max_steps=4 * 10 ** 6)
 
 
-@pytest.mark.parametrize("plant", ["end_waits_kv_only", "loader_no_acc_wait", "mma_no_acc_free_wait"])
+@pytest.mark.parametrize("plant", ["end_waits_kv_only", "loader_no_acc_wait", "mma_no_acc_free_wait",
+                                   "mma_cp_before_kv_wait", "loader_no_dq_item_wait"])
 def test_model_catches_planted_protocol_errors(plant):
     """Each planted mistake is caught as a hazard or an inexact parity wait on some
     schedule. The first is the end-of-list hand-off that waits only for the previous
     item's K/V copy: with items of at most four Q tiles the loader never blocks on the ring,
-    and the K/V barrier can run two phases ahead of the dQ warps."""
+    and the K/V barrier can run two phases ahead of a role. The fourth queues the K/V copy
+    into TMEM before the K/V in shared memory landed. The last starts an item without the dQ
+    warps' acknowledgement of the previous one: after a one-tile item every MMA can finish
+    while the dQ warps are still on the item before, and the K/V barrier runs two phases
+    ahead of them."""
     rng = random.Random(11)
     caught = 0
     for items in item_lists(rng, 100, short_only=True):
         for tc_weight in (1, 3):
-            for slow in (None, 4):  # every role at one speed, or warpgroup 1 lagging
+            for slow in (None, 1, 4):  # every role at one speed, or the dQ warps or warpgroup 1 lagging
                 try:
                     Model(items, random.Random(rng.random()), plant=plant, tc_weight=tc_weight, slow=slow).run()
                 except HazardError:
