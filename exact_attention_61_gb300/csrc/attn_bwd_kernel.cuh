@@ -17,7 +17,8 @@
 //    that see it (all of them, or those from the diagonal on under the causal
 //    mask). K and V stay in shared memory; Q, dO and the per-row LSE/D vectors
 //    stream through a TMA ring;
-//  - one warp issues the tcgen05 MMAs, all into tensor memory:
+//  - one warp issues the tcgen05 MMAs, all into tensor memory (at d = 64 after copying
+//    K and V into TMEM with tcgen05.cp, which the tensor core runs ahead of them):
 //      S^T  = K Q^T     (128 keys x 128 queries, fp32; d = 64: K from TMEM)
 //      dP^T = V dO^T    (128 x 128, fp32; d = 64: V from TMEM)
 //      dV  += P^T dO    (P^T 16-bit in TMEM over S^T; dO MN-major in SMEM)
@@ -145,11 +146,6 @@ __device__ __forceinline__ void mma_ts_k64_warp(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr)
-                 : "memory");
-}
-
 // Instruction descriptor with the major-ness of A chosen too (bit 15; A from SMEM).
 __host__ __device__ constexpr uint32_t idesc_f16_f32acc_ab(bool bf16, int M, int N, bool a_mn_major,
                                                            bool b_mn_major) {
@@ -235,8 +231,8 @@ struct BwdCfg {
     static constexpr int kBarDqFull = kBarPds + 2;         // dQ tile in TMEM
     static constexpr int kBarDqRead = kBarDqFull + 1;      // dQ tile read out
     static constexpr int kBarAcc = kBarDqRead + 1;         // dK, dV final
-    static constexpr int kBarKvTmem = kBarAcc + 1;         // d = 64: K and V copied into TMEM
-    static constexpr int kBarAccFree = kBarKvTmem + 1;     // persistent form: dK, dV read out
+    static constexpr int kBarDqItem = kBarAcc + 1;         // persistent form: the dQ warps read the item
+    static constexpr int kBarAccFree = kBarDqItem + 1;     // persistent form: dK, dV read out
     static constexpr int kBarDrain = kBarAccFree + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -333,7 +329,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages)
                 count = 1 + 8 + 1;  // MMA, compute warps, dQ store
             if (i == C::kBarPds || i == C::kBarPds + 1) count = C::kEarlyNext ? 4 : 8;  // compute warps
-            if (i == C::kBarDqRead || i == C::kBarKvTmem) count = 4;                     // dQ warps
+            if (i == C::kBarDqRead) count = 4;                                           // dQ warps
             mbar_init(bar(i), count);
         }
         misc[1] = 0u;
@@ -403,11 +399,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint64_t dQ_k0 = sdesc_sw128(sQ(0), 16, 1024);
         const uint64_t dQ_mn0 = sdesc_sw128(sQ(0), C::kBoxBytes, 1024);
 
-        // d = 64: the dQ warps copy K and V into TMEM once they have landed (which also
-        // means K is in shared memory for dQ).
-        bool ok = C::kKvTmem ? wait_warp(bar(C::kBarKvTmem), 0, wc, kRoleBwdMma * 1000 + C::kBarKvTmem, 0)
-                             : wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdMma * 1000 + C::kBarKV, 0);
+        bool ok = wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdMma * 1000 + C::kBarKV, 0);
         if (ok) tc_fence_after_sync();
+        // d = 64: K and V into TMEM, the A operands of S^T and dP^T (K stays in shared memory
+        // for dQ). The tensor core runs the MMAs issued after the copies behind them.
+        if constexpr (C::kKvTmem) {
+            if (ok && n_it > 0) {
+                tmem_cp_tile64_warp(tmem + C::colK, dK_k);
+                tmem_cp_tile64_warp(tmem + C::colV, dV_k);
+            }
+        }
         if constexpr (C::kEarlyNext) {
             // d = 64, per Q tile: for each half h (query columns [64h, 64h + 64), warpgroup
             // h), once its P^T/dS^T are ready: dV += P_h^T dO_h and dK += dS_h^T Q_h (K = 64
@@ -508,26 +509,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t lane_base = tmem_addr(tmem, wq * 32u, 0);
         const bool leader = warp == C::kWarpDq && lane == 0;
         if (leader) tma_prefetch_desc(&tmDQ);
-        if constexpr (C::kKvTmem) {
-            // K and V rows (128-byte-swizzled in shared memory) into TMEM lane r, 16-bit
-            // pairs per column: the A operands of S^T and dP^T.
-            const bool kv_ok = wait_warp(bar(C::kBarKV), 0, wc, kRoleBwdDq * 1000 + C::kBarKV, 0);
-            if (kv_ok) {
-#pragma unroll 1
-                for (int m = 0; m < 2; ++m) {
-                    const uint32_t row = base + (m ? C::kOffV : C::kOffK) + r * 128u;
-                    uint32_t x[32];
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        ld_shared_v4(row + ((ch ^ (r & 7u)) << 4), x[4 * ch], x[4 * ch + 1], x[4 * ch + 2], x[4 * ch + 3]);
-                    tmem_st32(lane_base + (m ? C::colV : C::colK), x);
-                }
-                tmem_st_wait();
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0 && kv_ok) mbar_arrive(bar(C::kBarKvTmem));
-        }
         for (int it = 0; it < n_it; ++it) {
             if (!wait_warp_sleep(bar(C::kBarDqFull), it & 1, wc, kRoleBwdDq * 1000 + C::kBarDqFull, it)) break;
             tc_fence_after_sync();

@@ -66,9 +66,6 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
     using C = BwdCfg<64>;
     constexpr int D = 64;
     static_assert(C::kEarlyNext && C::kKvTmem, "the persistent kernel is the d = 64 form");
-    // The one-item kernel's K/V-in-TMEM barrier; here the dQ warps arrive on it once they
-    // have read item k from the ring (they have passed their wait on the K/V barrier).
-    constexpr int kBarDqItem = C::kBarKvTmem;
     extern __shared__ __align__(1024) uint8_t smem_bwd[];
     const uint32_t base = smem_addr(smem_bwd);
     if (base & 1023u) {  // uniform over the CTA: nothing has been set up yet
@@ -96,7 +93,7 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
             uint32_t count = 1;
             if (i >= C::kBarQdEmpty && i < C::kBarQdEmpty + C::kStages) count = 1 + 8 + 1;  // MMA, compute, dQ store
             if (i == C::kBarPds || i == C::kBarPds + 1) count = 4;                         // a compute warpgroup
-            if (i == C::kBarDqRead || i == kBarDqItem) count = 4;                          // dQ warps
+            if (i == C::kBarDqRead || i == C::kBarDqItem) count = 4;                          // dQ warps
             if (i == C::kBarAccFree) count = 8;                                            // compute warps
             mbar_init(bar(i), count);
         }
@@ -143,7 +140,7 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
                 // is done (kBarAcc); the dQ warps by their own arrive (with one-tile items the
                 // MMAs can finish while the dQ warps are still on the item before). Then no
                 // role's parity wait can fall two phases behind.
-                if (k > 0 && !wait_one(bar(kBarDqItem), (k - 1) & 1, wc, kRoleBwdLoad * 1000 + 93, k)) break;
+                if (k > 0 && !wait_one(bar(C::kBarDqItem), (k - 1) & 1, wc, kRoleBwdLoad * 1000 + 93, k)) break;
                 if (x < 0) {
                     // No more items: complete the K/V barrier's next phase with no bytes so that
                     // the other roles read the -1. As for an item, only once every MMA of the
@@ -289,7 +286,7 @@ __global__ void __launch_bounds__(BwdCfg<64>::kThreads, 1)
             const int x = items[k & 3];
             if (x < 0) break;  // no more items
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarDqItem));
+            if (lane == 0) mbar_arrive(bar(C::kBarDqItem));
             int bh, kt;
             bwd_persist_item<CAUSAL>(x, p, bh, kt);
             const int qt0 = q_begin(kt);
